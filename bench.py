@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark: QLoRA linear forward + backward TFLOP/s on one GB300.
+
+One step = the forward of every linear of the workload, then the backward of
+each in reverse order (a training step's pass over these layers), on seeded
+synthetic inputs already resident in HBM.  Default workload: the Llama-3-8B
+MLP projections (gate and up 4096->14336, down 14336->4096) at 8192 packed
+tokens, rank 64, s = 0.25.  FLOPs counted per linear: 4MNK + 6Mr(K+N)
+(no frozen-weight gradient; dequantisation not counted).
+
+Prints one JSON line.  `--impl reference` times the CPU fp64 oracle instead,
+on a bounded sample of the same workload (that arm is a deliberately slow
+baseline, not a target).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from qlora_fine_tuning_gb300 import synth  # noqa: E402
+
+DEFAULT_WORKLOAD = "llama3-8b-mlp-m8192-4096x14336-r64"
+METRIC = "QLoRA linear fwd+bwd TFLOP/s on 1 GB300; % of BF16 dense tensor peak"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def workload_flops(lins) -> int:
+    return sum(synth.flops_fwd_bwd(li.M, li.N, li.K, li.r, len(li.seg_n)) for li in lins)
+
+
+def config_of(name, lins, n_gpus):
+    return {
+        "workload": name,
+        "linears": [{"label": li.meta.get("label"), "M": li.M, "K": li.K, "N": li.N, "r": li.r, "s": li.s,
+                     "n_seg": len(li.seg_n)} for li in lins],
+        "weights": "4-bit codebook indices + fp32 absmax per 64 (quantile codebook)",
+        "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
+        "l2": "inputs larger than L2 (per-step working set >> 129 MB), no flush",
+    }
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks only)
+# --------------------------------------------------------------------------
+
+def dist_init(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        import torch
+        if not torch.cuda.is_available():
+            backend = "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# clocks
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------------------
+# our CUDA path
+# --------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def run_ours(args, rank, world):
+    import torch
+    from qlora_fine_tuning_gb300 import binding
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    binding.lib()
+    lins = synth.workload(args.workload, seed=rank)
+    M_all = sum(li.M for li in lins)
+    flops = workload_flops(lins)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+    ws_bytes = max(binding.qlora_workspace_bytes(li.M, li.N, li.K, li.r, len(li.seg_n)) for li in lins)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    layers = []
+    for li in lins:
+        L = {"li": li}
+        L["idx"] = torch.from_numpy(li.idx).cuda()
+        L["absmax"] = torch.from_numpy(li.absmax).cuda()
+        L["codebook"] = torch.from_numpy(li.codebook).cuda()
+        L["w"] = binding.make_w4(L["idx"], L["absmax"], L["codebook"], li.N, li.K)
+        L["X"], L["A"], L["B"], L["dY"] = bf(li.X), bf(li.A), bf(li.B), bf(li.dY)
+        L["Y"] = torch.empty((li.M, li.N), dtype=torch.bfloat16, device="cuda")
+        L["XA"] = torch.empty((li.M, li.R), dtype=torch.bfloat16, device="cuda")
+        L["dX"] = torch.empty((li.M, li.K), dtype=torch.bfloat16, device="cuda")
+        L["dA"] = torch.empty((li.K, li.R), dtype=torch.float32, device="cuda")
+        L["dB"] = torch.empty((li.r, li.N), dtype=torch.float32, device="cuda")
+        L["seg"] = None if len(li.seg_n) == 1 else list(li.seg_n)
+        layers.append(L)
+    stream = torch.cuda.current_stream()
+
+    def step(Xs=None, dYs=None):
+        for i, L in enumerate(layers):
+            li = L["li"]
+            X = L["X"] if Xs is None else Xs[i]
+            binding.qlora_linear_fwd(X, li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["Y"], L["XA"], ws,
+                                     ws_bytes, stream)
+        for i in reversed(range(len(layers))):
+            L = layers[i]
+            li = L["li"]
+            X = L["X"] if Xs is None else Xs[i]
+            dY = L["dY"] if dYs is None else dYs[i]
+            binding.qlora_linear_bwd(dY, X, L["XA"], li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["dX"],
+                                     L["dA"], L["dB"], ws, ws_bytes, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = binding.qlora_check_device_error(ws)
+    if st != binding.OK:
+        raise RuntimeError(f"device error after warm-up: {binding.STATUS[st]}")
+
+    # ---- timed region: device-resident inputs ----
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    binding.qlora_profiler_enable(True)
+    binding.qlora_profiler_collect()
+    launches0 = binding.qlora_launch_counter()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = binding.qlora_launch_counter() - launches0
+    ms_total = ev0.elapsed_time(ev1)
+    kstats = binding.qlora_profiler_collect()
+    binding.qlora_profiler_enable(False)
+    clk = clocks.stop()
+    st = binding.qlora_check_device_error(ws)
+    if st != binding.OK:
+        raise RuntimeError(f"device error in timed region: {binding.STATUS[st]}")
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    value = flops * world / (ms_step * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel (the tcgen05 base GEMM) ----
+    peaks, peak_src = measured_peaks()
+    ktimes = {name: (n, ms) for name, n, ms in kstats}
+    main_flops_step = 0
+    for li in lins:
+        main_flops_step += 2 * li.M * li.N * li.K + 2 * li.M * li.r * li.N      # forward GEMM + rank-r steps
+        main_flops_step += 2 * li.M * li.N * li.K + 2 * li.M * li.R * li.K      # dX GEMM + rank-r steps
+    main_ms = sum(ktimes.get(k, (0, 0.0))[1] for k in ("gemm_fwd", "gemm_dx"))
+    main_launches = sum(ktimes.get(k, (0, 0.0))[0] for k in ("gemm_fwd", "gemm_dx"))
+    achieved = main_flops_step * args.steps / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    roofline = {
+        "kernel": "gemm_tc_kernel (forward Y and backward dX instances)",
+        "bound": "tensor",
+        "achieved": round(achieved, 2) if achieved else None,
+        "peak": peak,
+        "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+        "unit": "TFLOP/s",
+        "frac": round(achieved / peak, 4) if achieved else None,
+        "traffic": None,
+        "launches": main_launches,
+        "avg_launch_ms": round(main_ms / max(1, main_launches), 4),
+    }
+    total_kernel_ms = sum(ms for _, _, ms in kstats)
+    breakdown = {name: {"launches": n, "ms_per_step": round(ms / args.steps, 4),
+                        "share": round(ms / total_kernel_ms, 4) if total_kernel_ms else None}
+                 for name, n, ms in kstats}
+
+    # ---- end to end: pinned host inputs -> device, result gradients back ----
+    e2e = None
+    if not args.no_e2e:
+        hX = [torch.from_numpy(np.ascontiguousarray(L["li"].X).view(np.int16)).view(torch.bfloat16).pin_memory()
+              for L in layers]
+        hdY = [torch.from_numpy(np.ascontiguousarray(L["li"].dY).view(np.int16)).view(torch.bfloat16).pin_memory()
+               for L in layers]
+        dX_in = [torch.empty_like(L["X"]) for L in layers]
+        ddY_in = [torch.empty_like(L["dY"]) for L in layers]
+        hdA = [torch.empty(L["dA"].shape, dtype=torch.float32).pin_memory() for L in layers]
+        hdB = [torch.empty(L["dB"].shape, dtype=torch.float32).pin_memory() for L in layers]
+        h2d = sum(t.numel() * 2 for t in hX) + sum(t.numel() * 2 for t in hdY)
+        d2h = sum(t.numel() * 4 for t in hdA) + sum(t.numel() * 4 for t in hdB)
+
+        def e2e_step():
+            for i in range(len(layers)):
+                dX_in[i].copy_(hX[i], non_blocking=True)
+                ddY_in[i].copy_(hdY[i], non_blocking=True)
+            step(dX_in, ddY_in)
+            for i, L in enumerate(layers):
+                hdA[i].copy_(L["dA"], non_blocking=True)
+                hdB[i].copy_(L["dB"], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        ems = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+        e2e = {"value": round(flops * world / (ems * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(ems, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "what": "per step: X and dY of every linear copied from pinned host memory, fwd+bwd through "
+                       "the C ABI, dA and dB copied back"}
+        st = binding.qlora_check_device_error(ws)
+        if st != binding.OK:
+            raise RuntimeError(f"device error in e2e region: {binding.STATUS[st]}")
+
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; shapes and value distributions of the pages' workloads)",
+        "config": config_of(args.workload, lins, world),
+        "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
+        "roofline": roofline,
+        "kernels": breakdown,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    return out, lins
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle (baseline arm / reference arm)
+# --------------------------------------------------------------------------
+
+def oracle_sample_run(lins, rows_per_linear):
+    """fwd + bwd of every linear on its first `rows` tokens, fp64 oracle."""
+    import oracle
+    flops = 0
+    t0 = time.perf_counter()
+    for li in lins:
+        m = min(rows_per_linear, li.M)
+        _, w16 = oracle.dequant(li.idx, li.absmax, li.codebook, li.N, li.K)
+        X = oracle.bf16_to_f64(li.X[:m])
+        dY = oracle.bf16_to_f64(li.dY[:m])
+        seg = None if len(li.seg_n) == 1 else li.seg_n
+        oracle.linear_full(X, oracle.bf16_to_f64(w16), oracle.bf16_to_f64(li.A), oracle.bf16_to_f64(li.B), dY,
+                           li.r, li.s, seg_n=seg)
+        flops += synth.flops_fwd_bwd(m, li.N, li.K, li.r, len(li.seg_n))
+    return flops, time.perf_counter() - t0
+
+
+def cpu_baseline(lins, target_s):
+    import oracle
+    oracle.build()
+    f1, t1 = oracle_sample_run(lins, 2)  # calibration (includes the dequant of every weight)
+    rows = int(max(2, min(256, 2 * target_s / max(t1, 1e-3))))
+    f, t = oracle_sample_run(lins, rows)
+    return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"fwd+bwd of every linear on its first {rows} tokens (of {lins[0].M}); "
+                      f"{f / 1e9:.1f} GFLOP in {t:.1f} s, fp64, dequant included in the time",
+            "seconds": round(t, 2)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    lins = synth.workload(args.workload, seed=0)
+    import oracle
+    oracle.build()
+    # one step = the oracle's fwd+bwd over a bounded sample of the workload
+    f1, t1 = oracle_sample_run(lins, 2)
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(128, 2 * per_step / max(t1, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_run(lins, rows)
+    times, fl = [], 0
+    for _ in range(args.steps):
+        f, t = oracle_sample_run(lins, rows)
+        times.append(t)
+        fl = f
+    tot = sum(times)
+    value = fl * args.steps / tot / 1e12
+    ms_step = tot / args.steps * 1e3
+    sample = f"fwd+bwd of every linear on its first {rows} tokens (of {lins[0].M}), fp64 oracle"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(args.workload, lins, world),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world = dist_init(args.gpus)
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if rank == 0 and out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    out, lins = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            out["cpu_baseline"] = cpu_baseline(lins, args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

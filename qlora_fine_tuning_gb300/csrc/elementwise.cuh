@@ -1,0 +1,177 @@
+// elementwise.cuh -- HBM-bound kernels of the QLoRA linear path:
+//   * 4-bit -> bf16 (and fp32) dequantisation, row-major and transposed
+//   * small transposes of the rank-r operands
+//   * deterministic reductions of split partial sums
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace qlora {
+
+// deq(W)[n,k] = bf16( fp32( codebook[code(n,k)] * absmax[(n*K+k)/64] ) ).
+// code(n,k) is the low nibble of byte (n*K+k)/2 for even k, the high nibble
+// for odd k.  The fp32 product uses __fmul_rn (IEEE, subnormals kept) and
+// the bf16 rounding is round-to-nearest-even.
+//
+// Each thread converts 8 consecutive weights per step: one 32-bit load of 4
+// packed bytes, one absmax load (8 weights never straddle a 64-block), one
+// 16-byte bf16 store (and two 16-byte fp32 stores when requested).  A warp
+// thus reads 128 contiguous bytes and writes 512 contiguous bytes.
+__global__ void __launch_bounds__(256) dequant4_kernel(const uint32_t* __restrict__ idx4,
+                                                       const float* __restrict__ absmax,
+                                                       const float* __restrict__ codebook, int64_t n_groups,
+                                                       uint4* __restrict__ out_bf16,
+                                                       float4* __restrict__ out_f32) {
+  __shared__ float cb[16];
+  if (threadIdx.x < 16) cb[threadIdx.x] = codebook[threadIdx.x];
+  __syncthreads();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_groups; g += stride) {
+    const uint32_t packed = __ldg(idx4 + g);
+    const float am = __ldg(absmax + (g >> 3));  // 8 groups of 8 weights per 64-block
+    float w[8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t byte = (packed >> (8 * b)) & 0xFFu;
+      w[2 * b] = __fmul_rn(cb[byte & 0xFu], am);
+      w[2 * b + 1] = __fmul_rn(cb[byte >> 4], am);
+    }
+    if (out_bf16) {
+      uint4 o;
+      __nv_bfloat162 h0 = __floats2bfloat162_rn(w[0], w[1]);
+      __nv_bfloat162 h1 = __floats2bfloat162_rn(w[2], w[3]);
+      __nv_bfloat162 h2 = __floats2bfloat162_rn(w[4], w[5]);
+      __nv_bfloat162 h3 = __floats2bfloat162_rn(w[6], w[7]);
+      o.x = *reinterpret_cast<uint32_t*>(&h0);
+      o.y = *reinterpret_cast<uint32_t*>(&h1);
+      o.z = *reinterpret_cast<uint32_t*>(&h2);
+      o.w = *reinterpret_cast<uint32_t*>(&h3);
+      out_bf16[g] = o;
+    }
+    if (out_f32) {
+      out_f32[2 * g] = make_float4(w[0], w[1], w[2], w[3]);
+      out_f32[2 * g + 1] = make_float4(w[4], w[5], w[6], w[7]);
+    }
+  }
+}
+
+// Transposed dequantisation: outT[k,n] = deq(W)[n,k], outT is [K, N] with
+// row stride ldt elements.  One CTA converts a 64(n) x 64(k) tile through
+// shared memory so both the packed reads and the bf16 writes are coalesced.
+__global__ void __launch_bounds__(256) dequant4_t_kernel(const uint8_t* __restrict__ idx,
+                                                         const float* __restrict__ absmax,
+                                                         const float* __restrict__ codebook, int32_t N, int32_t K,
+                                                         __nv_bfloat16* __restrict__ outT, int64_t ldt) {
+  __shared__ float cb[16];
+  __shared__ __nv_bfloat16 tile[64][64 + 2];
+  if (threadIdx.x < 16) cb[threadIdx.x] = codebook[threadIdx.x];
+  __syncthreads();
+  const int n0 = blockIdx.y * 64;
+  const int k0 = blockIdx.x * 64;
+  // load: 64 rows x 32 bytes; thread t handles row t/4, bytes (t%4)*8 .. +8
+  {
+    const int rr = threadIdx.x >> 2;
+    const int cb8 = (threadIdx.x & 3) * 8;
+    const int n = n0 + rr;
+    if (n < N) {
+      const int64_t e0 = static_cast<int64_t>(n) * K + k0;
+      const uint2 pk = *reinterpret_cast<const uint2*>(idx + e0 / 2 + cb8);
+      const float am = absmax[e0 / 64];
+      const uint32_t words[2] = {pk.x, pk.y};
+#pragma unroll
+      for (int wi = 0; wi < 2; ++wi) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const uint32_t byte = (words[wi] >> (8 * b)) & 0xFFu;
+          const int kk = 2 * (cb8 + wi * 4 + b);
+          tile[rr][kk] = __float2bfloat16_rn(__fmul_rn(cb[byte & 0xFu], am));
+          tile[rr][kk + 1] = __float2bfloat16_rn(__fmul_rn(cb[byte >> 4], am));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) tile[rr][2 * cb8 + j] = __float2bfloat16_rn(0.f);
+    }
+  }
+  __syncthreads();
+  // store: 64 rows (k) x 64 (n); thread t writes k-row t/4, n (t%4)*16 .. +16
+  {
+    const int kr = threadIdx.x >> 2;
+    const int nc = (threadIdx.x & 3) * 16;
+    const int k = k0 + kr;
+    if (k < K) {
+      __nv_bfloat16* dst = outT + static_cast<int64_t>(k) * ldt + n0 + nc;
+      if (n0 + nc + 16 <= N) {
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          __nv_bfloat162 h;
+          h.x = tile[nc + 2 * j][kr];
+          h.y = tile[nc + 2 * j + 1][kr];
+          w[j] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else {
+        for (int j = 0; j < 16 && n0 + nc + j < N; ++j) dst[j] = tile[nc + j][kr];
+      }
+    }
+  }
+}
+
+// dst[c, rr] = src[rr, c] for rr < rows, c < cols; zero where dst_rows x
+// dst_cols extends beyond (padding).  Small operands only (rank-r sides).
+__global__ void transpose_pad_bf16_kernel(const __nv_bfloat16* __restrict__ src, int32_t rows, int32_t cols,
+                                          int64_t lds, __nv_bfloat16* __restrict__ dst, int32_t dst_rows,
+                                          int32_t dst_cols, int64_t ldd) {
+  __shared__ __nv_bfloat16 t[32][33];
+  const int r0 = blockIdx.x * 32;  // src rows = dst cols
+  const int c0 = blockIdx.y * 32;  // src cols = dst rows
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  for (int i = ty; i < 32; i += 8) {
+    const int rr = r0 + i, c = c0 + tx;
+    t[i][tx] = (rr < rows && c < cols) ? src[static_cast<int64_t>(rr) * lds + c] : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int dr = c0 + i, dc = r0 + tx;
+    if (dr < dst_rows && dc < dst_cols) dst[static_cast<int64_t>(dr) * ldd + dc] = t[tx][i];
+  }
+}
+
+// Sum of `splits` fp32 partials P[s][i][j] (i < rows, j < cols, row stride ld,
+// split stride sstride), in split order.  Writes any of:
+//   out_bf16[i][j]   = bf16(sum)            (ld_o)
+//   out_bf16_s[i][j] = bf16(scale * sum)    (ld_o)
+//   out_bf16_t[j][i] = bf16(sum)            (ld_t)
+//   out_f32[i][j]    = scale * sum          (ld_o)
+//   out_f32_t[j][i]  = scale * sum          (ld_t)
+struct ReduceArgs {
+  const float* part;
+  int32_t splits, rows, cols;
+  int64_t ld, sstride;
+  float scale;
+  __nv_bfloat16* out_bf16;
+  __nv_bfloat16* out_bf16_s;
+  __nv_bfloat16* out_bf16_t;
+  float* out_f32;
+  float* out_f32_t;
+  int64_t ld_o, ld_t;
+};
+
+__global__ void __launch_bounds__(256) reduce_splits_kernel(const ReduceArgs a) {
+  const int64_t total = static_cast<int64_t>(a.rows) * a.cols;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+    const int64_t i = e / a.cols, j = e % a.cols;
+    float acc = 0.f;
+    for (int s = 0; s < a.splits; ++s) acc += a.part[s * a.sstride + i * a.ld + j];
+    if (a.out_bf16) a.out_bf16[i * a.ld_o + j] = __float2bfloat16_rn(acc);
+    if (a.out_bf16_s) a.out_bf16_s[i * a.ld_o + j] = __float2bfloat16_rn(__fmul_rn(a.scale, acc));
+    if (a.out_bf16_t) a.out_bf16_t[j * a.ld_t + i] = __float2bfloat16_rn(acc);
+    if (a.out_f32) a.out_f32[i * a.ld_o + j] = __fmul_rn(a.scale, acc);
+    if (a.out_f32_t) a.out_f32_t[j * a.ld_t + i] = __fmul_rn(a.scale, acc);
+  }
+}
+
+}  // namespace qlora

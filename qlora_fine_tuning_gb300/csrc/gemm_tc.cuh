@@ -1,0 +1,288 @@
+// gemm_tc.cuh -- tcgen05 / TMEM / TMA GEMM for sm_103a.
+//
+// D[128-row tile, bn-col tile] = sum_red A[row, red] * B[col, red]
+//   (+ optional rank-r "LoRA" K-steps A2[row, :] * B2[col, :] into the same
+//    TMEM accumulator).
+//
+// Every contraction of the QLoRA linear layer is an instance:
+//   XA  = X . A            (A-op X K-major, B-op A^T)          fp32 split-K partials
+//   Y   = X . Wd^T + (s XA) . B    (B-op Wd; LoRA: A2 = s*XA, B2 = B^T)  bf16
+//   G   = dY . B^T per adapter segment                         fp32 split partials
+//   dX  = dY . Wd + (s G) . A^T    (B-op Wd^T; LoRA: A2 = s*G, B2 = A)  bf16
+//   dA  = X^T . G          (A-op X read MN-major, B-op G^T)    fp32 split partials
+//   dB^T= dY^T . XA        (A-op dY read MN-major, B-op XA^T)  fp32 split partials
+//
+// Roles (6 warps): warp 0 lane 0 issues TMA loads into a ring of `stages`
+// shared-memory stages; warp 1 lane 0 issues tcgen05.mma (M=128, N=bn, K=16)
+// into a TMEM accumulator; warps 2..5 wait for the accumulator, read it with
+// tcgen05.ld and store.  Warp 0 owns the TMEM allocation.
+//
+// Shared-memory tiles use the 128-byte swizzle written by TMA:
+//   K-major operand  : row i at i*128 B holds 64 reduction elements; 8-row
+//                      atoms of 1024 B (SBO = 1024); a 16-wide K step is +32 B.
+//   MN-major operand : row j at j*128 B holds 64 output-index elements for
+//                      reduction index j; 8-row atoms (SBO = 1024); the second
+//                      64-wide output block sits 8192 B further (LBO);
+//                      a 16-wide K step is +2048 B.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace qlora {
+
+enum GemmMode : int32_t {
+  GM_PLAIN = 0,  // no segments, no LoRA steps
+  GM_FWD = 1,    // LoRA steps; adapter segment chosen by the output-column tile
+  GM_G = 2,      // segment = blockIdx.z / splits; reduction over that segment's columns
+  GM_DX = 3,     // LoRA steps over all segments at once
+  GM_DB = 4,     // segment chosen by the output-row tile; B rows offset by seg*r
+};
+
+constexpr int kMaxSeg = 8;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kATileBytes = 128 * 128;  // 128 rows x 64 bf16
+
+struct GemmArgs {
+  int32_t M;          // output rows (masking)
+  int32_t N;          // output cols (masking, before out_col0)
+  int32_t bn;         // tile width = UMMA N (16..256, multiple of 16)
+  int32_t stages;     // ring depth (<= kMaxStages)
+  uint32_t stage_bytes;
+  int32_t mode;
+  int32_t red_len;    // reduction length in elements (modes other than GM_G)
+  int32_t splits;     // reduction splits (blockIdx.z % splits)
+  int32_t r;          // adapter rank
+  int32_t nseg;
+  int32_t seg_start[kMaxSeg + 1];  // segment boundaries over the layer's N
+  int32_t lora_atoms;   // number of 64-wide LoRA K blocks (0..4)
+  int32_t lora_ksteps;  // number of 16-wide LoRA K steps in total
+  int32_t out_ld;       // output row stride in elements
+  int32_t out_valid;    // columns n0+c >= out_valid are not stored
+  int64_t out_split_stride;  // elements between split partial outputs
+  void* out;
+  uint32_t* err;        // device error word (bit flags), may be null
+  uint64_t timeout_ns;  // bound on every barrier wait
+};
+
+__device__ __forceinline__ int seg_index(const GemmArgs& p, int pos) {
+  int sg = 0;
+#pragma unroll 1
+  for (int j = 1; j < p.nseg; ++j)
+    if (pos >= p.seg_start[j]) sg = j;
+  return sg;
+}
+
+__device__ __forceinline__ void report(const GemmArgs& p, uint32_t bit) {
+  if (p.err) atomicOr(p.err, bit);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool A_MN, bool OUT_F32>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                   const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((((raw + 1023u) & ~1023u)) - raw);
+  uint8_t* ctrl = smem + static_cast<uint32_t>(p.stages) * p.stage_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* accum = empty + kMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * 128;
+  const int n0 = blockIdx.y * p.bn;
+  const int split = blockIdx.z % p.splits;
+
+  int sg = 0;
+  if (p.mode == GM_FWD) sg = seg_index(p, n0);
+  else if (p.mode == GM_DB) sg = seg_index(p, m0);
+  else if (p.mode == GM_G) sg = blockIdx.z / p.splits;
+
+  int red_begin = 0, red_end = p.red_len;
+  if (p.mode == GM_G) {
+    red_begin = p.seg_start[sg];
+    red_end = p.seg_start[sg + 1];
+  }
+  const int nkb = (red_end - red_begin + 63) / 64;
+  const int chunk = (nkb + p.splits - 1) / p.splits;
+  const int kb0 = min(nkb, split * chunk);
+  const int kb1 = min(nkb, kb0 + chunk);
+  const int n_main = kb1 - kb0;
+  const bool has_lora = (p.mode == GM_FWD || p.mode == GM_DX) && p.lora_atoms > 0;
+  const int n_iter = n_main + (has_lora ? p.lora_atoms : 0);
+  const int b_row0 = n0 + (p.mode == GM_DB ? sg * p.r : 0);
+  const int a2_x0 = (p.mode == GM_FWD ? sg * p.r : 0);
+  const int out_col0 = (p.mode == GM_G ? sg * p.r : 0);
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < static_cast<uint32_t>(p.bn)) tmem_cols <<= 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(accum, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+  if (warp == 1 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (has_lora) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    const uint32_t tx = kATileBytes + static_cast<uint32_t>(p.bn) * 128u;
+    int issued = 0;
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % p.stages;
+      const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+      if (!mbar_wait(&empty[s], ph ^ 1u, p.timeout_ns)) {
+        report(p, 1u);
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      uint8_t* a_dst = smem + static_cast<uint32_t>(s) * p.stage_bytes;
+      uint8_t* b_dst = a_dst + kATileBytes;
+      mbar_arrive_expect_tx(&full[s], tx);
+      if (it < n_main) {
+        const int kel = red_begin + (kb0 + it) * 64;
+        if (A_MN) {
+          tma_load_2d(a_dst, &tmA, &full[s], m0, kel);
+          tma_load_2d(a_dst + 8192, &tmA, &full[s], m0 + 64, kel);
+        } else {
+          tma_load_2d(a_dst, &tmA, &full[s], kel, m0);
+        }
+        tma_load_2d(b_dst, &tmB, &full[s], kel, b_row0);
+      } else {
+        const int a = it - n_main;
+        tma_load_2d(a_dst, &tmA2, &full[s], a2_x0 + 64 * a, m0);
+        tma_load_2d(b_dst, &tmB2, &full[s], 64 * a, n0);
+      }
+      issued = it + 1;
+    }
+    // Do not leave the CTA while copies it issued may still land in smem.
+    for (int it = max(0, issued - p.stages); it < issued; ++it)
+      mbar_wait(&full[it % p.stages], static_cast<uint32_t>(it / p.stages) & 1u, p.timeout_ns);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc_main = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), A_MN, false);
+    const uint32_t idesc_lora = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), false, false);
+    for (int it = 0; it < n_iter; ++it) {
+      const int s = it % p.stages;
+      const uint32_t ph = static_cast<uint32_t>(it / p.stages) & 1u;
+      if (!mbar_wait(&full[s], ph, p.timeout_ns)) {
+        report(p, 2u);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_addr = smem_u32(smem + static_cast<uint32_t>(s) * p.stage_bytes);
+      const uint32_t b_addr = a_addr + kATileBytes;
+      const bool lora = it >= n_main;
+      const int ksteps = lora ? min(4, p.lora_ksteps - 4 * (it - n_main)) : 4;
+      for (int kk = 0; kk < ksteps; ++kk) {
+        uint64_t ad;
+        if (A_MN && !lora)
+          ad = sdesc_sw128(a_addr + static_cast<uint32_t>(kk) * 2048u, 8192u, 1024u);
+        else
+          ad = sdesc_sw128(a_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u);
+        const uint64_t bd = sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u);
+        tc_mma_bf16(tmem_base, ad, bd, lora ? idesc_lora : idesc_main, (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit(&empty[s]);
+    }
+    tc_commit(accum);  // arrives once every MMA issued above has completed
+  } else if (warp >= 2) {
+    // ---------------- Epilogue ----------------
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    const int grow = m0 + row;
+    bool ok = true;
+    if (!mbar_wait(accum, 0u, p.timeout_ns)) {
+      report(p, 4u);
+      ok = false;
+    }
+    tc_fence_after();
+    if (ok) {
+      const bool have_acc = n_iter > 0;
+      const bool row_ok = grow < p.M;
+      const int nchunks = p.bn / 16;
+      for (int j = 0; j < nchunks; ++j) {
+        uint32_t v[16];
+        if (have_acc) {
+          tmem_ld16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * 16), v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) v[t] = 0u;
+        }
+        const int c0 = n0 + j * 16;
+        if (!row_ok) continue;
+        if (OUT_F32) {
+          float* out = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(split) * p.out_split_stride +
+                       static_cast<int64_t>(grow) * p.out_ld + out_col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int c = c0 + g * 4;
+            if (c < p.out_valid && c < p.N) {
+              uint4 w = make_uint4(v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]);
+              *reinterpret_cast<uint4*>(out + c) = w;
+            }
+          }
+        } else {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(grow) * p.out_ld;
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            const int c = c0 + g * 8;
+            if (c < p.out_valid && c < p.N) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(v[g * 8 + 0]), __uint_as_float(v[g * 8 + 1]));
+              w.y = pack_bf16x2(__uint_as_float(v[g * 8 + 2]), __uint_as_float(v[g * 8 + 3]));
+              w.z = pack_bf16x2(__uint_as_float(v[g * 8 + 4]), __uint_as_float(v[g * 8 + 5]));
+              w.w = pack_bf16x2(__uint_as_float(v[g * 8 + 6]), __uint_as_float(v[g * 8 + 7]));
+              *reinterpret_cast<uint4*>(out + c) = w;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    // The accumulator barrier fires only after every issued MMA completed;
+    // it normally has already (the epilogue waited on it), but an epilogue
+    // that gave up early must not let the allocation go while MMAs run.
+    if (lane == 0) mbar_wait(accum, 0u, p.timeout_ns);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+}  // namespace qlora

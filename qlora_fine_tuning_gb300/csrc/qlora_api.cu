@@ -1,0 +1,649 @@
+// qlora_api.cu -- host side of libqlora.so: argument checks, workspace
+// carving, TMA descriptor encoding, launch sequencing, profiler.
+//
+// Forward (one call):
+//   dequant W -> Wd bf16 [N,K]            (elementwise, HBM-bound)
+//   A -> A^T [R,K], B -> B^T [N,Rp]       (tiny transposes; Rp = r rounded to 16)
+//   XA = X . A        tcgen05, split over K, fp32 partials -> XA_save, s*XA (bf16)
+//   Y  = X . Wd^T + (s*XA) . B   tcgen05, the rank-r product as extra K-steps
+//                                 into the same TMEM accumulator
+// Backward (one call):
+//   G  = dY . B^T per segment     tcgen05, split over N -> s*G [M,R], G^T [R,M]
+//   dequant W transposed -> Wd^T bf16 [K,N]
+//   dX = dY . Wd + (s*G) . A^T    tcgen05, rank-r product as extra K-steps
+//   dA = s X^T G      tcgen05 with X read MN-major, split over M
+//   dB = s XA^T dY    tcgen05 with dY read MN-major, split over M
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/qlora.h"
+#include "elementwise.cuh"
+#include "gemm_tc.cuh"
+
+using namespace qlora;
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Settings, profiler
+// ---------------------------------------------------------------------------
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<uint64_t> g_launches{0};
+
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pool_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Bracket one launch with events when the profiler is on.
+struct LaunchScope {
+  const char* name;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr, b = nullptr;
+  LaunchScope(const char* n, cudaStream_t s) : name(n), st(s) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_on) {
+      a = pool_event();
+      b = pool_event();
+      cudaEventRecord(a, st);
+    }
+  }
+  ~LaunchScope() {
+    if (a) {
+      cudaEventRecord(b, st);
+      std::lock_guard<std::mutex> lk(g_prof_mu);
+      g_prof_recs.push_back({name, a, b});
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// TMA descriptors (driver entry point fetched through the runtime, so the
+// library does not link libcuda directly)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] with row stride ld (elements), box
+// {64, box_outer}, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Shapes, workspace
+// ---------------------------------------------------------------------------
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+constexpr int kSMs = 152;
+constexpr int kMaxSplits = 8;
+
+// Split count that depends only on the reduction length, so that a row's
+// result never depends on how many rows are in the batch.
+int splits_for_rows(int64_t nkb) {
+  return static_cast<int>(std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, cdiv(nkb, 32))));
+}
+
+int choose_splits(int64_t tiles, int64_t nkb) {
+  int64_t s = std::max<int64_t>(1, (kSMs + tiles / 2) / std::max<int64_t>(1, tiles));
+  s = std::min<int64_t>(s, kMaxSplits);
+  s = std::min<int64_t>(s, std::max<int64_t>(1, nkb));
+  return static_cast<int>(s);
+}
+
+struct Layout {
+  int64_t M, N, K, r, nseg, R, Rp, Mp;
+  size_t off_err, off_wd, off_bt, off_at, off_xas, off_xat, off_gt, off_part, total;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+Layout layout(int64_t M, int64_t N, int64_t K, int64_t r, int64_t nseg) {
+  Layout L{};
+  L.M = M;
+  L.N = N;
+  L.K = K;
+  L.r = r;
+  L.nseg = nseg;
+  L.R = r * nseg;
+  L.Rp = rup(r, 16);
+  L.Mp = rup(std::max<int64_t>(M, 1), 8);
+  size_t o = 0;
+  L.off_err = o;
+  o += 256;
+  L.off_wd = o;
+  o = align256(o + size_t(N) * K * 2);
+  L.off_bt = o;
+  o = align256(o + size_t(N) * L.Rp * 2);
+  L.off_at = o;
+  o = align256(o + size_t(L.R) * K * 2);
+  L.off_xas = o;  // s*XA (forward) or s*G (backward), [M,R]
+  o = align256(o + size_t(std::max<int64_t>(M, 1)) * L.R * 2);
+  L.off_xat = o;  // XA^T [R, Mp]
+  o = align256(o + size_t(L.R) * L.Mp * 2);
+  L.off_gt = o;  // G^T [R, Mp]
+  o = align256(o + size_t(L.R) * L.Mp * 2);
+  L.off_part = o;
+  const int64_t pe = std::max({std::max<int64_t>(M, 1) * L.R, K * L.R, N * L.Rp});
+  o = align256(o + size_t(kMaxSplits) * pe * 4);
+  L.total = o;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Argument checks
+// ---------------------------------------------------------------------------
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+qlora_status check_w(const qlora_w4* w) {
+  if (!w || !w->idx || !w->absmax || !w->codebook) return QLORA_ERR_INVALID_ARG;
+  if (w->N < 0 || w->K < 0 || w->block != 64) return QLORA_ERR_INVALID_ARG;
+  if (w->K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (!al16(w->idx) || !al16(w->absmax) || !al16(w->codebook)) return QLORA_ERR_ALIGNMENT;
+  return QLORA_OK;
+}
+
+struct Segs {
+  int32_t n;
+  int32_t start[kMaxSeg + 1];
+};
+
+qlora_status check_layer(int64_t M, const qlora_w4* W, int32_t r, int32_t n_seg, const int64_t* seg_n, Segs* sg) {
+  qlora_status st = check_w(W);
+  if (st != QLORA_OK) return st;
+  if (M < 0) return QLORA_ERR_INVALID_ARG;
+  if (W->N < 8 || W->K < 64) return QLORA_ERR_INVALID_ARG;
+  if (W->N % 8 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (W->N > (int64_t(1) << 30) || W->K > (int64_t(1) << 30) || M > (int64_t(1) << 30))
+    return QLORA_ERR_UNSUPPORTED;
+  if (r < 8 || r > 128 || r % 8 != 0) return QLORA_ERR_INVALID_ARG;
+  if (n_seg < 1 || n_seg > kMaxSeg) return QLORA_ERR_INVALID_ARG;
+  if (int64_t(n_seg) * r > 256) return QLORA_ERR_UNSUPPORTED;
+  if (n_seg > 1 && !seg_n) return QLORA_ERR_INVALID_ARG;
+  sg->n = n_seg;
+  int64_t off = 0;
+  sg->start[0] = 0;
+  for (int j = 0; j < n_seg; ++j) {
+    const int64_t w = (n_seg == 1 && !seg_n) ? W->N : seg_n[j];
+    if (w <= 0) return QLORA_ERR_INVALID_ARG;
+    if (j < n_seg - 1 && w % 128 != 0) return QLORA_ERR_UNSUPPORTED;
+    off += w;
+    sg->start[j + 1] = static_cast<int32_t>(off);
+  }
+  if (off != W->N) return QLORA_ERR_INVALID_ARG;
+  return QLORA_OK;
+}
+
+qlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QLORA_OK : QLORA_ERR_CUDA; }
+
+// ---------------------------------------------------------------------------
+// Launch helpers
+// ---------------------------------------------------------------------------
+constexpr int kSmemLimit = 232448;
+
+struct TileCfg {
+  int bn, stages;
+  uint32_t stage_bytes;
+  size_t smem;
+};
+
+TileCfg tile_cfg(int bn) {
+  TileCfg c;
+  c.bn = bn;
+  c.stage_bytes = static_cast<uint32_t>(rup(kATileBytes + int64_t(bn) * 128, 1024));
+  c.stages = std::min<int>(kMaxStages, static_cast<int>((200 * 1024) / c.stage_bytes));
+  c.smem = size_t(c.stages) * c.stage_bytes + 1024 + 256;
+  return c;
+}
+
+template <bool A_MN, bool F32>
+qlora_status launch_gemm(const char* name, dim3 grid, const TileCfg& tc, const CUtensorMap& a, const CUtensorMap& b,
+                         const CUtensorMap& a2, const CUtensorMap& b2, GemmArgs args, cudaStream_t st) {
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(attr_once[dev & 63], [] {
+    cudaFuncSetAttribute(gemm_tc_kernel<A_MN, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  });
+  args.bn = tc.bn;
+  args.stages = tc.stages;
+  args.stage_bytes = tc.stage_bytes;
+  args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  {
+    LaunchScope ls(name, st);
+    gemm_tc_kernel<A_MN, F32><<<grid, 192, tc.smem, st>>>(a, b, a2, b2, args);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+GemmArgs base_args(uint32_t* err) {
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.splits = 1;
+  g.nseg = 1;
+  g.err = err;
+  return g;
+}
+
+qlora_status launch_dequant(const qlora_w4* w, void* out_bf16, float* out_f32, cudaStream_t st) {
+  const int64_t groups = w->N * w->K / 8;
+  if (groups == 0) return QLORA_OK;
+  const int64_t blocks = std::min<int64_t>(cdiv(groups, 256), int64_t(kSMs) * 16);
+  LaunchScope ls("dequant4", st);
+  dequant4_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      reinterpret_cast<const uint32_t*>(w->idx), w->absmax, w->codebook, groups, reinterpret_cast<uint4*>(out_bf16),
+      reinterpret_cast<float4*>(out_f32));
+  return cuda_status(cudaGetLastError());
+}
+
+qlora_status launch_transpose(const char* name, const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
+                              int64_t drows, int64_t dcols, int64_t ldd, cudaStream_t st) {
+  dim3 grid(static_cast<unsigned>(cdiv(dcols, 32)), static_cast<unsigned>(cdiv(drows, 32)));
+  LaunchScope ls(name, st);
+  transpose_pad_bf16_kernel<<<grid, 256, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(src), static_cast<int32_t>(rows), static_cast<int32_t>(cols), lds,
+      reinterpret_cast<__nv_bfloat16*>(dst), static_cast<int32_t>(drows), static_cast<int32_t>(dcols), ldd);
+  return cuda_status(cudaGetLastError());
+}
+
+qlora_status launch_reduce(const char* name, const ReduceArgs& ra, cudaStream_t st) {
+  const int64_t total = int64_t(ra.rows) * ra.cols;
+  if (total == 0) return QLORA_OK;
+  const int64_t blocks = std::min<int64_t>(cdiv(total, 256), int64_t(kSMs) * 8);
+  LaunchScope ls(name, st);
+  reduce_splits_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ra);
+  return cuda_status(cudaGetLastError());
+}
+
+ReduceArgs reduce_args(const float* part, int splits, int64_t rows, int64_t cols, int64_t ld, int64_t sstride,
+                       float scale) {
+  ReduceArgs ra;
+  std::memset(&ra, 0, sizeof(ra));
+  ra.part = part;
+  ra.splits = splits;
+  ra.rows = static_cast<int32_t>(rows);
+  ra.cols = static_cast<int32_t>(cols);
+  ra.ld = ld;
+  ra.sstride = sstride;
+  ra.scale = scale;
+  return ra;
+}
+
+#define QL_TRY(expr)                  \
+  do {                                \
+    qlora_status _s = (expr);         \
+    if (_s != QLORA_OK) return _s;    \
+  } while (0)
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+const char* qlora_status_str(qlora_status s) {
+  switch (s) {
+    case QLORA_OK: return "ok";
+    case QLORA_ERR_INVALID_ARG: return "invalid argument";
+    case QLORA_ERR_UNSUPPORTED: return "unsupported shape or parameter";
+    case QLORA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case QLORA_ERR_WORKSPACE: return "workspace missing or too small";
+    case QLORA_ERR_CUDA: return "CUDA error";
+    case QLORA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+void qlora_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(std::max<uint64_t>(ns, 1000000ull)); }
+
+void qlora_profiler_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+}
+
+uint64_t qlora_launch_counter(void) { return g_launches.load(); }
+
+int qlora_profiler_collect(qlora_kernel_stat* out, int max_entries) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof_recs);
+  }
+  std::vector<qlora_kernel_stat> stats;
+  for (const ProfRec& pr : recs) {
+    cudaEventSynchronize(pr.b);
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, pr.a, pr.b);
+    auto itr = std::find_if(stats.begin(), stats.end(),
+                            [&](const qlora_kernel_stat& k) { return std::strcmp(k.name, pr.name) == 0; });
+    if (itr == stats.end()) {
+      stats.push_back({pr.name, 1, static_cast<double>(ms)});
+    } else {
+      itr->launches += 1;
+      itr->total_ms += ms;
+    }
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (const ProfRec& pr : recs) {
+      g_event_pool.push_back(pr.a);
+      g_event_pool.push_back(pr.b);
+    }
+  }
+  for (int i = 0; i < static_cast<int>(stats.size()) && i < max_entries && out; ++i) out[i] = stats[i];
+  return static_cast<int>(stats.size());
+}
+
+size_t qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, int32_t n_seg) {
+  if (M < 0 || N <= 0 || K <= 0 || r <= 0 || n_seg <= 0) return 0;
+  return layout(M, N, K, r, n_seg).total;
+}
+
+qlora_status qlora_check_device_error(void* ws, cudaStream_t st) {
+  if (!ws) return QLORA_ERR_WORKSPACE;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QLORA_ERR_CUDA;
+  uint32_t flag = 0;
+  if (cudaMemcpy(&flag, ws, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return QLORA_ERR_CUDA;
+  if (flag != 0) {
+    if (cudaMemset(ws, 0, 4) != cudaSuccess) return QLORA_ERR_CUDA;
+    return QLORA_ERR_TIMEOUT;
+  }
+  return QLORA_OK;
+}
+
+qlora_status dequant_4bit(const qlora_w4* w, void* out_bf16, float* out_f32, cudaStream_t st) {
+  QL_TRY(check_w(w));
+  if (!out_bf16 && !out_f32) return QLORA_ERR_INVALID_ARG;
+  if ((out_bf16 && !al16(out_bf16)) || (out_f32 && !al16(out_f32))) return QLORA_ERR_ALIGNMENT;
+  return launch_dequant(w, out_bf16, out_f32, st);
+}
+
+qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const void* A, const void* B, int32_t r,
+                              int32_t n_seg, const int64_t* seg_n, float s, void* Y, void* XA_save, void* ws,
+                              size_t ws_bytes, cudaStream_t st) {
+  Segs sg;
+  QL_TRY(check_layer(M, W, r, n_seg, seg_n, &sg));
+  if (!X || !A || !B || !Y || !XA_save) return QLORA_ERR_INVALID_ARG;
+  if (!al16(X) || !al16(A) || !al16(B) || !al16(Y) || !al16(XA_save)) return QLORA_ERR_ALIGNMENT;
+  const int64_t N = W->N, K = W->K;
+  const Layout L = layout(M, N, K, r, n_seg);
+  if (!ws) return QLORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return QLORA_ERR_ALIGNMENT;
+  if (ws_bytes < L.total) return QLORA_ERR_WORKSPACE;
+  if (M == 0) return QLORA_OK;
+  if (!encode_fn()) return QLORA_ERR_CUDA;
+
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  uint32_t* err = reinterpret_cast<uint32_t*>(w8 + L.off_err);
+  void* Wd = w8 + L.off_wd;
+  void* Bt = w8 + L.off_bt;
+  void* At = w8 + L.off_at;
+  void* XAs = w8 + L.off_xas;
+  float* part = reinterpret_cast<float*>(w8 + L.off_part);
+  const int64_t R = L.R;
+
+  // 1. Wd = deq(W)
+  QL_TRY(launch_dequant(W, Wd, nullptr, st));
+  // 2. A^T [R,K], B^T [N,Rp] (zero columns r..Rp-1)
+  QL_TRY(launch_transpose("transpose_A", A, K, R, R, At, R, K, K, st));
+  QL_TRY(launch_transpose("transpose_B", B, r, N, N, Bt, N, L.Rp, L.Rp, st));
+
+  // 3. XA = X . A  (split over K)
+  CUtensorMap mX, mAt, mWd, mXAs, mBt;
+  {
+    const int bn = static_cast<int>(rup(R, 16));
+    const TileCfg tc = tile_cfg(bn);
+    const int64_t mt = cdiv(M, 128);
+    const int splits = splits_for_rows(K / 64);
+    if (!make_map(&mX, X, K, M, K, 128) || !make_map(&mAt, At, K, R, K, static_cast<uint32_t>(bn)))
+      return QLORA_ERR_CUDA;
+    GemmArgs g = base_args(err);
+    g.M = static_cast<int32_t>(M);
+    g.N = static_cast<int32_t>(R);
+    g.mode = GM_PLAIN;
+    g.red_len = static_cast<int32_t>(K);
+    g.splits = splits;
+    g.out_ld = static_cast<int32_t>(R);
+    g.out_valid = static_cast<int32_t>(R);
+    g.out_split_stride = M * R;
+    g.out = part;
+    QL_TRY((launch_gemm<false, true>("gemm_xa", dim3(static_cast<unsigned>(mt), 1, splits), tc, mX, mAt, mX, mAt, g,
+                                     st)));
+    ReduceArgs ra = reduce_args(part, splits, M, R, R, M * R, s);
+    ra.out_bf16 = reinterpret_cast<__nv_bfloat16*>(XA_save);
+    ra.out_bf16_s = reinterpret_cast<__nv_bfloat16*>(XAs);
+    ra.ld_o = R;
+    QL_TRY(launch_reduce("reduce_xa", ra, st));
+  }
+
+  // 4. Y = X . Wd^T + (s XA) . B
+  {
+    bool b256 = true;
+    for (int j = 1; j < n_seg; ++j)
+      if (sg.start[j] % 256 != 0) b256 = false;
+    const int bn = b256 ? 256 : 128;
+    const TileCfg tc = tile_cfg(bn);
+    if (!make_map(&mWd, Wd, K, N, K, static_cast<uint32_t>(bn)) || !make_map(&mXAs, XAs, R, M, R, 128) ||
+        !make_map(&mBt, Bt, L.Rp, N, L.Rp, static_cast<uint32_t>(bn)))
+      return QLORA_ERR_CUDA;
+    GemmArgs g = base_args(err);
+    g.M = static_cast<int32_t>(M);
+    g.N = static_cast<int32_t>(N);
+    g.mode = GM_FWD;
+    g.red_len = static_cast<int32_t>(K);
+    g.r = r;
+    g.nseg = n_seg;
+    for (int j = 0; j <= n_seg; ++j) g.seg_start[j] = sg.start[j];
+    g.lora_ksteps = static_cast<int32_t>(L.Rp / 16);
+    g.lora_atoms = static_cast<int32_t>(cdiv(L.Rp, 64));
+    g.out_ld = static_cast<int32_t>(N);
+    g.out_valid = static_cast<int32_t>(N);
+    g.out = Y;
+    dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(N, bn)), 1);
+    QL_TRY((launch_gemm<false, false>("gemm_fwd", grid, tc, mX, mWd, mXAs, mBt, g, st)));
+  }
+  return QLORA_OK;
+}
+
+qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_saved, int64_t M, const qlora_w4* W,
+                              const void* A, const void* B, int32_t r, int32_t n_seg, const int64_t* seg_n, float s,
+                              void* dX, float* dA, float* dB, void* ws, size_t ws_bytes, cudaStream_t st) {
+  Segs sg;
+  QL_TRY(check_layer(M, W, r, n_seg, seg_n, &sg));
+  if (!dY || !X || !XA_saved || !A || !B || !dA || !dB) return QLORA_ERR_INVALID_ARG;
+  if (!al16(dY) || !al16(X) || !al16(XA_saved) || !al16(A) || !al16(B) || !al16(dA) || !al16(dB) ||
+      (dX && !al16(dX)))
+    return QLORA_ERR_ALIGNMENT;
+  const int64_t N = W->N, K = W->K;
+  const Layout L = layout(M, N, K, r, n_seg);
+  if (!ws) return QLORA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return QLORA_ERR_ALIGNMENT;
+  if (ws_bytes < L.total) return QLORA_ERR_WORKSPACE;
+  const int64_t R = L.R;
+  if (M == 0) {
+    QL_TRY(cuda_status(cudaMemsetAsync(dA, 0, size_t(K) * R * 4, st)));
+    QL_TRY(cuda_status(cudaMemsetAsync(dB, 0, size_t(r) * N * 4, st)));
+    return QLORA_OK;
+  }
+  if (!encode_fn()) return QLORA_ERR_CUDA;
+
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  uint32_t* err = reinterpret_cast<uint32_t*>(w8 + L.off_err);
+  void* WdT = w8 + L.off_wd;
+  void* Gs = w8 + L.off_xas;
+  void* XAt = w8 + L.off_xat;
+  void* Gt = w8 + L.off_gt;
+  float* part = reinterpret_cast<float*>(w8 + L.off_part);
+
+  CUtensorMap mdY, mB, mWdT, mGs, mA, mXmn, mGt, mdYmn, mXAt;
+
+  // 1. G = dY . B^T per segment (split over the segment's columns)
+  {
+    const int bn = static_cast<int>(rup(r, 16));
+    const TileCfg tc = tile_cfg(bn);
+    const int64_t mt = cdiv(M, 128);
+    int64_t min_nkb = INT64_MAX;
+    for (int j = 0; j < n_seg; ++j) min_nkb = std::min<int64_t>(min_nkb, cdiv(sg.start[j + 1] - sg.start[j], 64));
+    const int splits = static_cast<int>(std::min<int64_t>(splits_for_rows(min_nkb), min_nkb));
+    if (!make_map(&mdY, dY, N, M, N, 128) || !make_map(&mB, B, N, r, N, static_cast<uint32_t>(bn)))
+      return QLORA_ERR_CUDA;
+    GemmArgs g = base_args(err);
+    g.M = static_cast<int32_t>(M);
+    g.N = r;
+    g.mode = GM_G;
+    g.splits = splits;
+    g.r = r;
+    g.nseg = n_seg;
+    for (int j = 0; j <= n_seg; ++j) g.seg_start[j] = sg.start[j];
+    g.out_ld = static_cast<int32_t>(R);
+    g.out_valid = r;
+    g.out_split_stride = M * R;
+    g.out = part;
+    QL_TRY((launch_gemm<false, true>("gemm_g", dim3(static_cast<unsigned>(mt), 1, splits * n_seg), tc, mdY, mB, mdY,
+                                     mB, g, st)));
+    ReduceArgs ra = reduce_args(part, splits, M, R, R, M * R, s);
+    ra.out_bf16_s = reinterpret_cast<__nv_bfloat16*>(Gs);
+    ra.out_bf16_t = reinterpret_cast<__nv_bfloat16*>(Gt);
+    ra.ld_o = R;
+    ra.ld_t = L.Mp;
+    QL_TRY(launch_reduce("reduce_g", ra, st));
+  }
+
+  // 2. dX = dY . Wd + (s G) . A^T
+  if (dX) {
+    {
+      dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(cdiv(N, 64)));
+      LaunchScope ls("dequant4_t", st);
+      dequant4_t_kernel<<<grid, 256, 0, st>>>(W->idx, W->absmax, W->codebook, static_cast<int32_t>(N),
+                                              static_cast<int32_t>(K), reinterpret_cast<__nv_bfloat16*>(WdT), N);
+      QL_TRY(cuda_status(cudaGetLastError()));
+    }
+    const int bn = 256;
+    const TileCfg tc = tile_cfg(bn);
+    if (!make_map(&mWdT, WdT, N, K, N, static_cast<uint32_t>(bn)) || !make_map(&mGs, Gs, R, M, R, 128) ||
+        !make_map(&mA, A, R, K, R, static_cast<uint32_t>(bn)))
+      return QLORA_ERR_CUDA;
+    GemmArgs g = base_args(err);
+    g.M = static_cast<int32_t>(M);
+    g.N = static_cast<int32_t>(K);
+    g.mode = GM_DX;
+    g.red_len = static_cast<int32_t>(N);
+    g.r = r;
+    g.nseg = n_seg;
+    g.lora_ksteps = static_cast<int32_t>(cdiv(R, 16));
+    g.lora_atoms = static_cast<int32_t>(cdiv(R, 64));
+    g.out_ld = static_cast<int32_t>(K);
+    g.out_valid = static_cast<int32_t>(K);
+    g.out = dX;
+    dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(K, bn)), 1);
+    QL_TRY((launch_gemm<false, false>("gemm_dx", grid, tc, mdY, mWdT, mGs, mA, g, st)));
+  }
+
+  // 3. dA = s X^T G   (X read MN-major, split over M)
+  {
+    const int bn = static_cast<int>(rup(R, 16));
+    const TileCfg tc = tile_cfg(bn);
+    const int64_t kt = cdiv(K, 128);
+    const int splits = choose_splits(kt, cdiv(M, 64));
+    if (!make_map(&mXmn, X, K, M, K, 64) || !make_map(&mGt, Gt, M, R, L.Mp, static_cast<uint32_t>(bn)))
+      return QLORA_ERR_CUDA;
+    GemmArgs g = base_args(err);
+    g.M = static_cast<int32_t>(K);
+    g.N = static_cast<int32_t>(R);
+    g.mode = GM_PLAIN;
+    g.red_len = static_cast<int32_t>(M);
+    g.splits = splits;
+    g.out_ld = static_cast<int32_t>(R);
+    g.out_valid = static_cast<int32_t>(R);
+    g.out_split_stride = K * R;
+    g.out = part;
+    QL_TRY((launch_gemm<true, true>("gemm_da", dim3(static_cast<unsigned>(kt), 1, splits), tc, mXmn, mGt, mXmn, mGt,
+                                    g, st)));
+    ReduceArgs ra = reduce_args(part, splits, K, R, R, K * R, s);
+    ra.out_f32 = dA;
+    ra.ld_o = R;
+    QL_TRY(launch_reduce("reduce_da", ra, st));
+  }
+
+  // 4. dB = s XA^T dY  (computed as dB^T = dY^T . XA with dY read MN-major)
+  {
+    QL_TRY(launch_transpose("transpose_XA", XA_saved, M, R, R, XAt, R, L.Mp, L.Mp, st));
+    const int bn = static_cast<int>(rup(r, 16));
+    const TileCfg tc = tile_cfg(bn);
+    const int64_t nt = cdiv(N, 128);
+    const int splits = choose_splits(nt, cdiv(M, 64));
+    if (!make_map(&mdYmn, dY, N, M, N, 64) || !make_map(&mXAt, XAt, M, R, L.Mp, static_cast<uint32_t>(bn)))
+      return QLORA_ERR_CUDA;
+    GemmArgs g = base_args(err);
+    g.M = static_cast<int32_t>(N);
+    g.N = r;
+    g.mode = GM_DB;
+    g.red_len = static_cast<int32_t>(M);
+    g.splits = splits;
+    g.r = r;
+    g.nseg = n_seg;
+    for (int j = 0; j <= n_seg; ++j) g.seg_start[j] = sg.start[j];
+    g.out_ld = r;
+    g.out_valid = r;
+    g.out_split_stride = N * r;
+    g.out = part;
+    QL_TRY((launch_gemm<true, true>("gemm_db", dim3(static_cast<unsigned>(nt), 1, splits), tc, mdYmn, mXAt, mdYmn,
+                                    mXAt, g, st)));
+    ReduceArgs ra = reduce_args(part, splits, N, r, r, N * r, s);
+    ra.out_f32_t = dB;
+    ra.ld_t = N;
+    QL_TRY(launch_reduce("reduce_db", ra, st));
+  }
+  return QLORA_OK;
+}
+
+}  // extern "C"

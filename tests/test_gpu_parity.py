@@ -1,0 +1,234 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on seeded inputs.
+
+Bar: dequantisation bit-exact; Y, dX, dA, dB within 1e-2 relative Frobenius
+error (bf16 operands, fp32 accumulation, bf16 Y/dX); exact zeros where the
+definition gives exact zeros.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from qlora_fine_tuning_gb300 import binding, synth
+
+from golden_case import expected_dense, load as load_golden
+from harness import (GpuLayer, TOL, compare, dev, host_bits, oracle_full, oracle_sampled,
+                     sample_indices)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.lib()
+    yield
+
+
+# --------------------------------------------------------------------------
+# dequantisation: bit-exact
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K,kind", [(8, 64, "U"), (1024, 1024, "Q"), (24, 4160, "Q"), (4096, 4096, "Q")])
+def test_dequant_bit_exact(N, K, kind):
+    import torch
+    li = synth.make_linear(1, N, K, 8, 1.0, cb_kind=kind, seed=N + K)
+    w = binding.make_w4(dev(li.idx), dev(li.absmax), dev(li.codebook), N, K)
+    ob = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    of = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    keep = (w,)
+    binding.dequant_4bit(w, ob, of)
+    torch.cuda.synchronize()
+    w32, w16 = oracle.dequant(li.idx, li.absmax, li.codebook, N, K)
+    assert np.array_equal(host_bits(ob), w16)
+    assert np.array_equal(of.cpu().numpy().view(np.uint32), w32.view(np.uint32))
+    del keep
+
+
+def test_dequant_edge_scales_bit_exact():
+    import torch
+    cb = synth.codebook("Q")
+    vals = [0.0, 1.0, 0.02, 2.0 ** -126, float(np.finfo(np.float32).max), float(np.float32(1e-45)), 3.0, 7.5e-39]
+    N, K = len(vals), 64
+    codes = np.tile(np.arange(16, dtype=np.uint8), K // 16)
+    idx = np.tile(codes[0::2] | (codes[1::2] << 4), (N, 1)).astype(np.uint8)
+    absmax = np.array(vals, dtype=np.float32)
+    w = binding.make_w4(dev(idx), dev(absmax), dev(cb), N, K)
+    ob = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    of = torch.empty((N, K), dtype=torch.float32, device="cuda")
+    binding.dequant_4bit(w, ob, of)
+    torch.cuda.synchronize()
+    w32, w16 = oracle.dequant(idx, absmax, cb, N, K)
+    assert np.array_equal(host_bits(ob), w16)
+    assert np.array_equal(of.cpu().numpy().view(np.uint32), w32.view(np.uint32))
+
+
+# --------------------------------------------------------------------------
+# hand-worked example: exact
+# --------------------------------------------------------------------------
+
+def test_golden_closed_form_exact():
+    c = load_golden()
+    r = 8  # the ABI's smallest rank: pad the rank-1 example with zero columns/rows
+    M, K, N = c["M"], c["K"], c["N"]
+    A = np.zeros((K, r), dtype=np.float32)
+    A[:, 0] = c["A"][:, 0]
+    B = np.zeros((r, N), dtype=np.float32)
+    B[0] = c["B"][0]
+    li = synth.LinearInputs(M=M, N=N, K=K, r=r, s=c["s"], seg_n=(N,), idx=c["idx"], absmax=c["absmax"],
+                            codebook=c["codebook"], X=synth.to_bf16_bits(c["X"]), A=synth.to_bf16_bits(A),
+                            B=synth.to_bf16_bits(B), dY=synth.to_bf16_bits(c["dY"]))
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    g.check()
+    got = g.results()
+    e = c["expect"]
+    _, dx_exp, da_exp = expected_dense(c)
+    assert np.array_equal(got["Y"], e["Y"])
+    assert np.array_equal(got["XA"][:, :1], e["XA"]) and np.all(got["XA"][:, 1:] == 0)
+    assert np.array_equal(got["dX"], dx_exp)
+    assert np.array_equal(got["dA"][:, :1], da_exp) and np.all(got["dA"][:, 1:] == 0)
+    assert np.array_equal(got["dB"][:1], e["dB"]) and np.all(got["dB"][1:] == 0)
+
+
+# --------------------------------------------------------------------------
+# small shapes, full comparison
+# --------------------------------------------------------------------------
+
+SMALL = [
+    # M, N, K, r, s, seg_n
+    (256, 1024, 1024, 8, 2.0, None),          # the tiny workload
+    (1, 64, 64, 8, 1.0, None),                # single row, single k-block
+    (100, 136, 192, 16, 0.5, None),           # ragged M and N tails
+    (129, 264, 128, 32, 1.0, None),           # one row past a tile, N past a 256 tile
+    (300, 512, 256, 64, 0.25, None),
+    (130, 384, 128, 128, 2.0, None),          # largest rank: two 64-wide LoRA blocks
+    (200, 320, 128, 16, 1.0, (128, 128, 64)), # three adapters side by side
+    (64, 384, 192, 8, 2.0, (256, 128)),       # rank 8 with two adapters
+]
+
+
+@pytest.mark.parametrize("M,N,K,r,s,seg", SMALL)
+def test_small_shapes_match_oracle(M, N, K, r, s, seg):
+    li = synth.make_linear(M, N, K, r, s, seg_n=seg, seed=M * 7 + N)
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    g.check()
+    got = g.results()
+    ref = oracle_full(li)
+    compare(got, ref, keys=("Y", "dX", "dA", "dB", "XA"))
+
+
+@pytest.mark.parametrize("variant", ["w_zero", "b_large", "u_codebook"])
+def test_lora_visible_variants(variant):
+    """W = 0 makes Y and dX pure LoRA; B ~ N(0,1) makes the LoRA term dominate."""
+    kw = dict(M=192, N=256, K=256, r=16, s=2.0, seed=11)
+    if variant == "w_zero":
+        kw["w_zero"] = True
+    elif variant == "b_large":
+        kw["b_std"] = 1.0
+    else:
+        kw["cb_kind"] = "U"
+    li = synth.make_linear(**kw)
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    g.check()
+    compare(g.results(), oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
+
+
+def test_b_zero_gives_exact_zero_da_and_a_zero_gives_exact_zero_db():
+    li = synth.make_linear(160, 256, 128, 16, 1.0, b_zero=True, seed=3)
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    g.check()
+    got = g.results()
+    assert np.all(got["dA"] == 0.0)
+    li = synth.make_linear(160, 256, 128, 16, 1.0, a_zero=True, seed=4)
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    g.check()
+    got = g.results()
+    assert np.all(got["dB"] == 0.0) and np.all(got["XA"] == 0.0)
+
+
+def test_empty_batch():
+    import torch
+    li = synth.make_linear(1, 64, 64, 8, 1.0)
+    g = GpuLayer(li)
+    g.dA.fill_(7.0)
+    g.dB.fill_(7.0)
+    binding.qlora_linear_fwd(g.X, 0, g.w, g.A, g.B, 8, None, 1.0, g.Y, g.XA, g.ws, g.ws_bytes)
+    binding.qlora_linear_bwd(g.dY, g.X, g.XA, 0, g.w, g.A, g.B, 8, None, 1.0, g.dX, g.dA, g.dB, g.ws, g.ws_bytes)
+    torch.cuda.synchronize()
+    assert float(g.dA.abs().max()) == 0.0 and float(g.dB.abs().max()) == 0.0
+
+
+def test_deterministic_repeat():
+    li = synth.make_linear(300, 384, 256, 16, 1.0, seed=21)
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    a = g.results()
+    g.forward()
+    g.backward()
+    b = g.results()
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_rows_independent_of_batch_split():
+    """Packed sequences: a row's Y and dX do not depend on the other rows."""
+    li = synth.make_linear(512, 256, 256, 16, 1.0, seed=5, with_lengths=True)
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    full = g.results()
+    off = 0
+    for L in li.lengths[:3]:
+        sub = synth.LinearInputs(M=int(L), N=li.N, K=li.K, r=li.r, s=li.s, seg_n=li.seg_n, idx=li.idx,
+                                 absmax=li.absmax, codebook=li.codebook, X=li.X[off:off + L], A=li.A, B=li.B,
+                                 dY=li.dY[off:off + L])
+        gs = GpuLayer(sub)
+        gs.forward()
+        gs.backward()
+        part = gs.results()
+        assert np.array_equal(part["Y"], full["Y"][off:off + L])
+        assert np.array_equal(part["dX"], full["dX"][off:off + L])
+        off += int(L)
+
+
+# --------------------------------------------------------------------------
+# the pages' workloads at full size, sampled outputs
+# --------------------------------------------------------------------------
+
+FULL = [
+    ("llama3-8b-q_proj-m4096-k4096-n4096-r16", 0),
+    ("llama3-8b-qkv-gqa-m8192-k4096-n6144-r16x3", 0),
+    ("llama3-8b-mlp-m8192-4096x14336-r64", 0),   # gate
+    ("llama3-8b-mlp-m8192-4096x14336-r64", 2),   # down
+    ("qwen3-14b-mlp-m16384-5120x17408-r16", 0),  # gate
+]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,which", FULL)
+def test_full_size_sampled(name, which):
+    label, kw = synth.WORKLOADS[name][which]
+    li = synth.make_linear(seed=0, stream=which, **kw)
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    g.check()
+    got = g.results()
+    idx = sample_indices(li)
+    rows, kidx, Jidx, cidx, nidx = idx
+    ref = oracle_sampled(li, idx)
+    sub = {"Y": got["Y"][rows], "dX": got["dX"][rows], "XA": got["XA"][rows],
+           "dA": got["dA"][np.ix_(kidx, Jidx)], "dB": got["dB"][np.ix_(cidx, nidx)]}
+    compare(sub, ref, keys=("Y", "dX", "dA", "dB", "XA"))
