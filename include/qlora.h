@@ -138,6 +138,32 @@ int qlora_profiler_collect(qlora_kernel_stat* out, int max_entries);
 /* Number of kernels launched by this library since load (profiler or not). */
 uint64_t qlora_launch_counter(void);
 
+/* ---- XA = X A without a caller-provided workspace ----
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory themselves -- for example a plug-in
+ * whose host application owns every device allocation, or a loop that must
+ * not go through the allocator -- and so cannot provide the workspace the
+ * other entry points need.
+ * Computes XA bf16 [M,R] = bf16(X A) for X bf16 [M,K] and A bf16 [K,R], the
+ * same values qlora_linear_fwd writes to XA_save (R = n_seg * r there).
+ * Its scratch is a static device array of QLORA_XA_STATIC_SCRATCH_BYTES
+ * (8 MiB) that every GPU which loads the library holds until the process
+ * exits.  The first call on a device looks the array's address up on that
+ * device (make that first call before any stream capture).  All calls share
+ * the array and it keeps the last call's contents: calls that can overlap on
+ * the GPU (different streams, or several host threads) race -- order them on
+ * one stream.  Nothing in the array has to start at zero.  The call
+ * allocates nothing.  Sizes whose A^T (2 R K bytes) plus the fp32 partial
+ * sums of 128 rows do not fit in the array are rejected with
+ * QLORA_ERR_WORKSPACE (for example K = 16384 with R = 256); larger M is
+ * processed in row chunks.  A device-side wait that runs out is not reported
+ * by this entry point (XA is then unspecified).
+ * Preconditions: K % 64 == 0, 8 <= R <= 256, R % 8 == 0, 16-byte aligned
+ * pointers.  Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
+#define QLORA_XA_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t K, const void* A, int32_t R, void* XA,
+                                    cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -87,6 +87,8 @@ def lib(path: Optional[str] = None):
             L.qlora_profiler_collect.argtypes = [ctypes.POINTER(KernelStat), ctypes.c_int]
             L.qlora_launch_counter.restype = ctypes.c_uint64
             L.qlora_launch_counter.argtypes = []
+            L.qlora_linear_xa_static.restype = ctypes.c_int
+            L.qlora_linear_xa_static.argtypes = [P, I64, I64, P, I32, P, P]
             _lib = L
     return _lib
 
@@ -188,6 +190,13 @@ def qlora_profiler_collect() -> list:
 
 def qlora_launch_counter() -> int:
     return int(lib().qlora_launch_counter())
+
+
+def qlora_linear_xa_static(X, M: int, K: int, A, R: int, XA, stream=None) -> None:
+    """XA = X A with the library's static device scratch: for callers that
+    cannot allocate device memory, so cannot provide a workspace."""
+    st = lib().qlora_linear_xa_static(_ptr(X), int(M), int(K), _ptr(A), int(R), _ptr(XA), _stream(stream))
+    _check(st, "qlora_linear_xa_static")
 
 
 # --------------------------------------------------------------------------

@@ -647,3 +647,82 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// XA = X A with scratch in a static device array (for callers that cannot
+// allocate the workspace).  Same kernels, same split count and tile order as
+// the forward's XA step, so the result equals qlora_linear_fwd's XA_save.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_xa_static_scratch[QLORA_XA_STATIC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_xa_static_mu;
+void* g_xa_static_addr[64] = {};
+
+// Device address of the static array on the current device, looked up once
+// per device with that device current.
+qlora_status xa_static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return QLORA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_xa_static_mu);
+  if (!g_xa_static_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_xa_static_scratch) != cudaSuccess || !p) return QLORA_ERR_CUDA;
+    g_xa_static_addr[dev] = p;
+  }
+  *out = g_xa_static_addr[dev];
+  return QLORA_OK;
+}
+}  // namespace
+
+extern "C" qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t K, const void* A, int32_t R,
+                                               void* XA, cudaStream_t st) {
+  if (!X || !A || !XA) return QLORA_ERR_INVALID_ARG;
+  if (M < 0 || K < 64 || R < 8 || R > 256 || R % 8 != 0) return QLORA_ERR_INVALID_ARG;
+  if (K % 64 != 0 || K > (int64_t(1) << 30) || M > (int64_t(1) << 30)) return QLORA_ERR_UNSUPPORTED;
+  if (!al16(X) || !al16(A) || !al16(XA)) return QLORA_ERR_ALIGNMENT;
+  const size_t cap = QLORA_XA_STATIC_SCRATCH_BYTES;
+  const int splits = splits_for_rows(K / 64);
+  const size_t at_bytes = align256(size_t(R) * K * 2);
+  const size_t per_row = size_t(splits) * R * 4;
+  if (at_bytes + 128 * per_row > cap) return QLORA_ERR_WORKSPACE;
+  if (M == 0) return QLORA_OK;
+  int64_t rows_per_chunk = static_cast<int64_t>((cap - at_bytes) / per_row) / 128 * 128;
+  rows_per_chunk = std::min<int64_t>(rows_per_chunk, rup(M, 128));
+  void* base = nullptr;
+  QL_TRY(xa_static_scratch(&base));
+  if (!encode_fn()) return QLORA_ERR_CUDA;
+  uint8_t* b8 = static_cast<uint8_t*>(base);
+  void* At = b8;
+  float* part = reinterpret_cast<float*>(b8 + at_bytes);
+
+  QL_TRY(launch_transpose("transpose_A_static", A, K, R, R, At, R, K, K, st));
+  const int bn = static_cast<int>(rup(R, 16));
+  const TileCfg tc = tile_cfg(bn);
+  CUtensorMap mAt;
+  if (!make_map(&mAt, At, K, R, K, static_cast<uint32_t>(bn))) return QLORA_ERR_CUDA;
+  for (int64_t m0 = 0; m0 < M; m0 += rows_per_chunk) {
+    const int64_t mc = std::min<int64_t>(rows_per_chunk, M - m0);
+    const void* Xc = static_cast<const uint8_t*>(X) + size_t(m0) * K * 2;
+    CUtensorMap mX;
+    if (!make_map(&mX, Xc, K, mc, K, 128)) return QLORA_ERR_CUDA;
+    GemmArgs g = base_args(nullptr);
+    g.M = static_cast<int32_t>(mc);
+    g.N = R;
+    g.mode = GM_PLAIN;
+    g.red_len = static_cast<int32_t>(K);
+    g.splits = splits;
+    g.out_ld = R;
+    g.out_valid = R;
+    g.out_split_stride = mc * R;
+    g.out = part;
+    QL_TRY((launch_gemm<false, true>("gemm_xa_static", dim3(static_cast<unsigned>(cdiv(mc, 128)), 1, splits), tc, mX,
+                                     mAt, mX, mAt, g, st)));
+    ReduceArgs ra = reduce_args(part, splits, mc, R, R, mc * R, 1.0f);
+    ra.out_bf16 = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(XA) + size_t(m0) * R * 2);
+    ra.ld_o = R;
+    QL_TRY(launch_reduce("reduce_xa_static", ra, st));
+  }
+  return QLORA_OK;
+}
