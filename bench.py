@@ -38,8 +38,8 @@ METRIC = "QLoRA linear fwd+bwd TFLOP/s on 1 GB300; % of BF16 dense tensor peak"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
-    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-e2e", action="store_true")
@@ -334,6 +334,7 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded numpy PCG64; shapes and value distributions of the pages' workloads)",
         "config": config_of(args.workload, lins, world),
         "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
+        "pct_of_bf16_peak_burst": round(100.0 * value / world / float(peaks.get("bf16_tflops", peak)), 2),
         "roofline": roofline,
         "kernels": breakdown,
         "gpu_launches": int(launches),
@@ -367,8 +368,14 @@ def oracle_sample_run(lins, rows_per_linear):
 def cpu_baseline(lins, target_s):
     import oracle
     oracle.build()
-    f1, t1 = oracle_sample_run(lins, 2)  # calibration (includes the dequant of every weight)
-    rows = int(max(2, min(256, 2 * target_s / max(t1, 1e-3))))
+    # calibration: the dequant of every weight is a fixed cost, the rows add linearly
+    # (rows >= the thread count, so both calibration runs keep every core busy)
+    nt = max(1, oracle.num_threads())
+    r1, r2 = nt, 2 * nt
+    _, t1 = oracle_sample_run(lins, r1)
+    _, t2 = oracle_sample_run(lins, r2)
+    per_row = max((t2 - t1) / (r2 - r1), 1e-4)
+    rows = int(max(r1, min(1024, r1 + (target_s - t1) / per_row)))
     f, t = oracle_sample_run(lins, rows)
     return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"fwd+bwd of every linear on its first {rows} tokens (of {lins[0].M}); "

@@ -123,6 +123,16 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 constexpr int kSMs = 152;
+
+// Number of SMs of device `dev` (cached; 152 on GB300).
+int sm_count(int dev) {
+  static std::atomic<int> cache[64];
+  int v = cache[dev & 63].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = kSMs;
+  cache[dev & 63].store(v, std::memory_order_relaxed);
+  return v;
+}
 constexpr int kMaxSplits = 8;
 
 // Split count that depends only on the reduction length, so that a row's
@@ -256,9 +266,15 @@ qlora_status launch_gemm(const char* name, dim3 grid, const TileCfg& tc, const C
   args.stages = tc.stages;
   args.stage_bytes = tc.stage_bytes;
   args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  // `grid` is the tile grid; the kernel is persistent with one CTA per SM.
+  args.m_tiles = static_cast<int32_t>(grid.x);
+  args.n_tiles = static_cast<int32_t>(grid.y);
+  args.z_tiles = static_cast<int32_t>(grid.z);
+  const int64_t tiles = int64_t(grid.x) * grid.y * grid.z;
+  const unsigned ctas = static_cast<unsigned>(std::min<int64_t>(tiles, sm_count(dev)));
   {
     LaunchScope ls(name, st);
-    gemm_tc_kernel<A_MN, F32><<<grid, 192, tc.smem, st>>>(a, b, a2, b2, args);
+    gemm_tc_kernel<A_MN, F32><<<ctas, 192, tc.smem, st>>>(a, b, a2, b2, args);
   }
   return cuda_status(cudaGetLastError());
 }
