@@ -124,7 +124,11 @@ def _check(st: int, where: str):
 
 
 def make_w4(idx, absmax, codebook, N: int, K: int, block: int = 64) -> W4:
-    return W4(_ptr(idx), _ptr(absmax), _ptr(codebook), int(N), int(K), int(block))
+    """Descriptor of a 4-bit weight.  It keeps references to the tensors it
+    points at, so their device memory outlives the descriptor."""
+    w = W4(_ptr(idx), _ptr(absmax), _ptr(codebook), int(N), int(K), int(block))
+    w._keep = (idx, absmax, codebook)
+    return w
 
 
 def _seg_array(seg_n: Optional[Sequence[int]]):

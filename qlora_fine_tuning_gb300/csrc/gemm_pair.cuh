@@ -1,0 +1,246 @@
+// gemm_pair.cuh -- persistent tcgen05 GEMM on CTA pairs (.cta_group::2) for
+// the two large contractions of the layer:
+//   Y  = X . Wd^T + (s XA) . B       and      dX = dY . Wd + (s G) . A^T
+// Both operands K-major, bf16 output.
+//
+// A cluster of two CTAs computes a 256 x 256 output tile with one
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=16) per 16-wide K step: each CTA
+// holds 128 rows of A and 128 rows of B (half of N) in its own shared memory,
+// and the accumulator rows of each CTA live in its own TMEM.  Compared with a
+// single-CTA 128 x 256 tile this halves the B bytes each SM stages and feeds
+// to the tensor core per K step, which is what bounds the single-CTA kernel.
+//
+// Roles per CTA (6 warps; issuing roles run as whole warps and one elected
+// lane issues, keeping every operand warp-uniform):
+//   warp 0         TMA producer for this CTA's halves; completion is counted
+//                  on the even CTA's "full" barrier (it expects both halves);
+//   warp 1         (even CTA only) MMA issuer; commits multicast to both
+//                  CTAs' "empty" / "accumulator full" barriers;
+//   warps 2..5     epilogue for this CTA's 128 rows; release the accumulator
+//                  by arriving on the even CTA's "accumulator empty" barrier.
+// Two TMEM accumulators of 256 columns (512 columns, allocated for the pair).
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "gemm_tc.cuh"
+#include "ptx.cuh"
+
+namespace qlora {
+
+constexpr uint32_t kPairStageBytes = 2 * 128 * 128;  // A half + B half, 64-wide K block
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                     const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((((raw + 1023u) & ~1023u)) - raw);
+  uint8_t* ctrl = smem + static_cast<uint32_t>(p.stages) * kPairStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* tfull = empty + kMaxStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int npairs = static_cast<int>(gridDim.x >> 1);
+  const int total = p.m_tiles * p.n_tiles;
+  const bool has_lora = p.lora_atoms > 0;
+  const int nkb = (p.red_len + 63) / 64;
+  constexpr uint32_t kAccCols = 256;
+  constexpr uint32_t kTmemCols = 512;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (warp == 1 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (has_lora) {
+      tma_prefetch_desc(&tmA2);
+      tma_prefetch_desc(&tmB2);
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);      // even CTA's ring barriers
+  const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);  // even CTA's accumulator-empty
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs; whole warp, elected lane issues) ----------------
+    const uint32_t tx_pair = 2u * kPairStageBytes;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int tile = pair; tile < total && ok; tile += npairs) {
+      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      const int m0 = mt * 256 + static_cast<int>(rank) * 128;  // this CTA's rows of A / output
+      const int nb = nt * 256;
+      const int n0 = nb + static_cast<int>(rank) * 128;        // this CTA's rows of B
+      const int sg = (p.mode == GM_FWD) ? seg_index(p, nb) : 0;
+      const int a2_x0 = (p.mode == GM_FWD) ? sg * p.r : 0;
+      const int n_iter = nkb + (has_lora ? p.lora_atoms : 0);
+      for (int it = 0; it < n_iter; ++it) {
+        const uint32_t s = g % static_cast<uint32_t>(p.stages);
+        const uint32_t ph = (g / static_cast<uint32_t>(p.stages)) & 1u;
+        if (!warp_wait(&empty[s], ph ^ 1u, p.timeout_ns, abort_flag)) {
+          if (lane == 0) {
+            if (!*abort_flag) report(p, 1u);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        uint8_t* a_dst = smem + s * kPairStageBytes;
+        uint8_t* b_dst = a_dst + kATileBytes;
+        const uint32_t bar = full0 + s * 8u;
+        if (rank == 0) mbar_arrive_expect_tx_ws(&full[s], tx_pair);
+        if (it < nkb) {
+          const int kel = it * 64;
+          tma_load_2d_pair_ws(a_dst, &tmA, bar, kel, m0);
+          tma_load_2d_pair_ws(b_dst, &tmB, bar, kel, n0);
+        } else {
+          const int a = it - nkb;
+          tma_load_2d_pair_ws(a_dst, &tmA2, bar, a2_x0 + 64 * a, m0);
+          tma_load_2d_pair_ws(b_dst, &tmB2, bar, 64 * a, n0);
+        }
+        ++g;
+      }
+    }
+    if (rank == 0 && lane == 0) {
+      const uint32_t S = static_cast<uint32_t>(p.stages);
+      for (uint32_t q = (g > S ? g - S : 0u); q < g; ++q) mbar_wait(&full[q % S], (q / S) & 1u, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (even CTA; whole warp, elected lane issues) ----------------
+    if (rank == 0) {
+      const uint32_t idesc = idesc_bf16_f32(256, 256, false, false);
+      uint32_t g = 0;
+      int j = 0;
+      bool ok = true;
+      for (int tile = pair; tile < total && ok; tile += npairs, ++j) {
+        const uint32_t acc = static_cast<uint32_t>(j & 1);
+        if (!warp_wait(&tempty[acc], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
+          if (lane == 0) {
+            if (!*abort_flag) report(p, 8u);
+            *abort_flag = 1;
+          }
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kAccCols;
+        const int n_iter = nkb + (has_lora ? p.lora_atoms : 0);
+        for (int it = 0; it < n_iter; ++it) {
+          const uint32_t s = g % static_cast<uint32_t>(p.stages);
+          const uint32_t ph = (g / static_cast<uint32_t>(p.stages)) & 1u;
+          if (!warp_wait(&full[s], ph, p.timeout_ns, abort_flag)) {
+            if (lane == 0) {
+              if (!*abort_flag) report(p, 2u);
+              *abort_flag = 1;
+            }
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * kPairStageBytes);
+          const uint32_t b_addr = a_addr + kATileBytes;
+          if (it < nkb) {
+            tc_mma_bf16_pair_k64_ws(d_tmem, sdesc_sw128(a_addr, 16u, 1024u), sdesc_sw128(b_addr, 16u, 1024u), 2u, 2u,
+                                    idesc, it > 0 ? 1u : 0u);
+          } else {
+            const int ksteps = min(4, p.lora_ksteps - 4 * (it - nkb));
+            for (int kk = 0; kk < ksteps; ++kk)
+              tc_mma_bf16_pair_ws(d_tmem, sdesc_sw128(a_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u),
+                                  sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u), idesc,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit_pair_multicast_ws(&empty[s], 0x3);
+          ++g;
+        }
+        if (!ok) break;
+        tc_commit_pair_multicast_ws(&tfull[acc], 0x3);
+      }
+      tc_commit_pair_multicast_ws(mma_done, 0x3);
+    }
+  } else if (warp >= 2) {
+    // ---------------- Epilogue (both CTAs, own 128 rows) ----------------
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    int j = 0;
+    for (int tile = pair; tile < total; tile += npairs, ++j) {
+      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      const uint32_t acc = static_cast<uint32_t>(j & 1);
+      if (!warp_wait(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
+        if (lane == 0) {
+          if (!*abort_flag) report(p, 4u);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const int grow = mt * 256 + static_cast<int>(rank) * 128 + row;
+      const bool row_ok = grow < p.M;
+      const uint32_t t_base = tmem_base + acc * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(grow) * p.out_ld;
+      for (int c = 0; c < 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(t_base + static_cast<uint32_t>(c * 16), v);
+        tmem_ld_wait();
+        if (!row_ok) continue;
+        const int c0 = nt * 256 + c * 16;
+#pragma unroll
+        for (int gq = 0; gq < 2; ++gq) {
+          const int col = c0 + gq * 8;
+          if (col < p.N) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[gq * 8 + 0]), __uint_as_float(v[gq * 8 + 1]));
+            w.y = pack_bf16x2(__uint_as_float(v[gq * 8 + 2]), __uint_as_float(v[gq * 8 + 3]));
+            w.z = pack_bf16x2(__uint_as_float(v[gq * 8 + 4]), __uint_as_float(v[gq * 8 + 5]));
+            w.w = pack_bf16x2(__uint_as_float(v[gq * 8 + 6]), __uint_as_float(v[gq * 8 + 7]));
+            *reinterpret_cast<uint4*>(out + col) = w;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(&tempty[acc]);
+        else mbar_arrive_cluster(tempty0 + acc * 8u);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0 && lane == 0) mbar_wait(mma_done, 0u, p.timeout_ns);  // no MMA still writes our TMEM
+  __syncwarp();
+  cluster_sync_all();  // the peer is done with the pair's TMEM too
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace qlora

@@ -16,7 +16,7 @@
 // tile, then split/segment) with stride gridDim.x.  Roles (6 warps):
 //   warp 0 lane 0  TMA producer, runs ahead across tile boundaries through a
 //                  ring of `stages` shared-memory stages;
-//   warp 1 lane 0  MMA issuer: tcgen05.mma (M=128, N=bn, K=16) into one of two
+//   warp 1         MMA issuer: tcgen05.mma (M=128, N=bn, K=16) into one of two
 //                  TMEM accumulators (tile j uses buffer j&1);
 //   warps 2..5     epilogue: tcgen05.ld of the finished accumulator, convert,
 //                  store; then release the buffer -- so the epilogue of tile j
@@ -194,8 +194,8 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0) {
+    // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
     const uint32_t tx = kATileBytes + static_cast<uint32_t>(p.bn) * 128u;
     uint32_t g = 0;  // iterations issued so far (ring position)
     bool ok = true;
@@ -204,48 +204,56 @@ __global__ void __launch_bounds__(192, 1)
       for (int it = 0; it < t.n_iter; ++it) {
         const uint32_t s = g % static_cast<uint32_t>(p.stages);
         const uint32_t ph = (g / static_cast<uint32_t>(p.stages)) & 1u;
-        if (!wait_or_abort(&empty[s], ph ^ 1u, p.timeout_ns, abort_flag)) {
-          if (!*abort_flag) report(p, 1u);
-          *abort_flag = 1;
+        if (!warp_wait(&empty[s], ph ^ 1u, p.timeout_ns, abort_flag)) {
+          if (lane == 0) {
+            if (!*abort_flag) report(p, 1u);
+            *abort_flag = 1;
+          }
           ok = false;
           break;
         }
         uint8_t* a_dst = smem + s * p.stage_bytes;
         uint8_t* b_dst = a_dst + kATileBytes;
-        mbar_arrive_expect_tx(&full[s], tx);
+        mbar_arrive_expect_tx_ws(&full[s], tx);
         if (it < t.n_main) {
           const int kel = t.red_begin + (t.kb0 + it) * 64;
           if (A_MN) {
-            tma_load_2d(a_dst, &tmA, &full[s], t.m0, kel);
-            tma_load_2d(a_dst + 8192, &tmA, &full[s], t.m0 + 64, kel);
+            tma_load_2d_ws(a_dst, &tmA, &full[s], t.m0, kel);
+            tma_load_2d_ws(a_dst + 8192, &tmA, &full[s], t.m0 + 64, kel);
           } else {
-            tma_load_2d(a_dst, &tmA, &full[s], kel, t.m0);
+            tma_load_2d_ws(a_dst, &tmA, &full[s], kel, t.m0);
           }
-          tma_load_2d(b_dst, &tmB, &full[s], kel, t.b_row0);
+          tma_load_2d_ws(b_dst, &tmB, &full[s], kel, t.b_row0);
         } else {
           const int a = it - t.n_main;
-          tma_load_2d(a_dst, &tmA2, &full[s], t.a2_x0 + 64 * a, t.m0);
-          tma_load_2d(b_dst, &tmB2, &full[s], 64 * a, t.n0);
+          tma_load_2d_ws(a_dst, &tmA2, &full[s], t.a2_x0 + 64 * a, t.m0);
+          tma_load_2d_ws(b_dst, &tmB2, &full[s], 64 * a, t.n0);
         }
         ++g;
       }
     }
     // Do not leave the CTA while copies it issued may still land in smem.
-    const uint32_t S = static_cast<uint32_t>(p.stages);
-    for (uint32_t q = (g > S ? g - S : 0u); q < g; ++q) mbar_wait(&full[q % S], (q / S) & 1u, p.timeout_ns);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t S = static_cast<uint32_t>(p.stages);
+      for (uint32_t q = (g > S ? g - S : 0u); q < g; ++q) mbar_wait(&full[q % S], (q / S) & 1u, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
     const uint32_t idesc_main = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), A_MN, false);
     const uint32_t idesc_lora = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), false, false);
+    const uint64_t a_step = A_MN ? (2048u >> 4) : (32u >> 4);
     uint32_t g = 0;
     int j = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++j) {
       const TileInfo t = tile_info(p, tile);
       const uint32_t acc = static_cast<uint32_t>(j & 1);
-      if (!wait_or_abort(&tempty[acc], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
-        if (!*abort_flag) report(p, 8u);
-        *abort_flag = 1;
+      if (!warp_wait(&tempty[acc], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
+        if (lane == 0) {
+          if (!*abort_flag) report(p, 8u);
+          *abort_flag = 1;
+        }
         break;
       }
       tc_fence_after();
@@ -253,33 +261,35 @@ __global__ void __launch_bounds__(192, 1)
       for (int it = 0; it < t.n_iter; ++it) {
         const uint32_t s = g % static_cast<uint32_t>(p.stages);
         const uint32_t ph = (g / static_cast<uint32_t>(p.stages)) & 1u;
-        if (!wait_or_abort(&full[s], ph, p.timeout_ns, abort_flag)) {
-          if (!*abort_flag) report(p, 2u);
-          *abort_flag = 1;
+        if (!warp_wait(&full[s], ph, p.timeout_ns, abort_flag)) {
+          if (lane == 0) {
+            if (!*abort_flag) report(p, 2u);
+            *abort_flag = 1;
+          }
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t a_addr = smem_u32(smem + s * p.stage_bytes);
         const uint32_t b_addr = a_addr + kATileBytes;
-        const bool lora = it >= t.n_main;
-        const int ksteps = lora ? min(4, p.lora_ksteps - 4 * (it - t.n_main)) : 4;
-        for (int kk = 0; kk < ksteps; ++kk) {
-          uint64_t ad;
-          if (A_MN && !lora)
-            ad = sdesc_sw128(a_addr + static_cast<uint32_t>(kk) * 2048u, 8192u, 1024u);
-          else
-            ad = sdesc_sw128(a_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u);
-          const uint64_t bd = sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u);
-          tc_mma_bf16(d_tmem, ad, bd, lora ? idesc_lora : idesc_main, (it > 0 || kk > 0) ? 1u : 0u);
+        if (it < t.n_main) {
+          const uint64_t ad = A_MN ? sdesc_sw128(a_addr, 8192u, 1024u) : sdesc_sw128(a_addr, 16u, 1024u);
+          tc_mma_bf16_k64_ws(d_tmem, ad, sdesc_sw128(b_addr, 16u, 1024u), a_step, 2u, idesc_main,
+                             it > 0 ? 1u : 0u);
+        } else {
+          const int ksteps = min(4, p.lora_ksteps - 4 * (it - t.n_main));
+          for (int kk = 0; kk < ksteps; ++kk)
+            tc_mma_bf16_ws(d_tmem, sdesc_sw128(a_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u),
+                           sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u), idesc_lora,
+                           (it > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&empty[s]);
+        tc_commit_ws(&empty[s]);
         ++g;
       }
       if (!ok) break;
-      tc_commit(&tfull[acc]);  // arrives once this tile's MMAs have completed
+      tc_commit_ws(&tfull[acc]);  // arrives once this tile's MMAs have completed
     }
-    tc_commit(mma_done);
+    tc_commit_ws(mma_done);
   } else if (warp >= 2) {
     // ---------------- Epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -288,9 +298,11 @@ __global__ void __launch_bounds__(192, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++j) {
       const TileInfo t = tile_info(p, tile);
       const uint32_t acc = static_cast<uint32_t>(j & 1);
-      if (!wait_or_abort(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
-        if (!*abort_flag) report(p, 4u);
-        *abort_flag = 1;
+      if (!warp_wait(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
+        if (lane == 0) {
+          if (!*abort_flag) report(p, 4u);
+          *abort_flag = 1;
+        }
         break;
       }
       tc_fence_after();

@@ -17,6 +17,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -25,6 +26,7 @@
 
 #include "../../include/qlora.h"
 #include "elementwise.cuh"
+#include "gemm_pair.cuh"
 #include "gemm_tc.cuh"
 
 using namespace qlora;
@@ -279,6 +281,39 @@ qlora_status launch_gemm(const char* name, dim3 grid, const TileCfg& tc, const C
   return cuda_status(cudaGetLastError());
 }
 
+// CTA-pair kernel for the two large GEMMs (256 x 256 tiles, K-major operands).
+constexpr int kPairStages = 6;
+
+bool pair_enabled() {
+  const char* e = std::getenv("QLORA_DISABLE_PAIR");
+  return !(e && e[0] == '1');
+}
+
+qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles, const CUtensorMap& a,
+                              const CUtensorMap& b, const CUtensorMap& a2, const CUtensorMap& b2, GemmArgs args,
+                              cudaStream_t st) {
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t smem = size_t(kPairStages) * kPairStageBytes + 1024 + 256;
+  std::call_once(attr_once[dev & 63], [smem] {
+    cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  });
+  args.bn = 256;
+  args.stages = kPairStages;
+  args.stage_bytes = kPairStageBytes;
+  args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  args.m_tiles = static_cast<int32_t>(m_tiles);
+  args.n_tiles = static_cast<int32_t>(n_tiles);
+  args.z_tiles = 1;
+  const int64_t pairs = std::min<int64_t>(m_tiles * n_tiles, sm_count(dev) / 2);
+  {
+    LaunchScope ls(name, st);
+    gemm_pair_kernel<<<static_cast<unsigned>(2 * pairs), 192, smem, st>>>(a, b, a2, b2, args);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
 GemmArgs base_args(uint32_t* err) {
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
@@ -486,10 +521,12 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     bool b256 = true;
     for (int j = 1; j < n_seg; ++j)
       if (sg.start[j] % 256 != 0) b256 = false;
+    const bool pair = b256 && pair_enabled();
     const int bn = b256 ? 256 : 128;
     const TileCfg tc = tile_cfg(bn);
-    if (!make_map(&mWd, Wd, K, N, K, static_cast<uint32_t>(bn)) || !make_map(&mXAs, XAs, R, M, R, 128) ||
-        !make_map(&mBt, Bt, L.Rp, N, L.Rp, static_cast<uint32_t>(bn)))
+    const uint32_t brows = pair ? 128u : static_cast<uint32_t>(bn);  // rows of B staged per CTA
+    if (!make_map(&mWd, Wd, K, N, K, brows) || !make_map(&mXAs, XAs, R, M, R, 128) ||
+        !make_map(&mBt, Bt, L.Rp, N, L.Rp, brows))
       return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(M);
@@ -504,8 +541,12 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     g.out_ld = static_cast<int32_t>(N);
     g.out_valid = static_cast<int32_t>(N);
     g.out = Y;
-    dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(N, bn)), 1);
-    QL_TRY((launch_gemm<false, false>("gemm_fwd", grid, tc, mX, mWd, mXAs, mBt, g, st)));
+    if (pair) {
+      QL_TRY(launch_gemm_pair("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, g, st));
+    } else {
+      dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(N, bn)), 1);
+      QL_TRY((launch_gemm<false, false>("gemm_fwd", grid, tc, mX, mWd, mXAs, mBt, g, st)));
+    }
   }
   return QLORA_OK;
 }
@@ -585,8 +626,10 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     }
     const int bn = 256;
     const TileCfg tc = tile_cfg(bn);
-    if (!make_map(&mWdT, WdT, N, K, N, static_cast<uint32_t>(bn)) || !make_map(&mGs, Gs, R, M, R, 128) ||
-        !make_map(&mA, A, R, K, R, static_cast<uint32_t>(bn)))
+    const bool pair = pair_enabled();
+    const uint32_t brows = pair ? 128u : static_cast<uint32_t>(bn);
+    if (!make_map(&mWdT, WdT, N, K, N, brows) || !make_map(&mGs, Gs, R, M, R, 128) ||
+        !make_map(&mA, A, R, K, R, brows))
       return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(M);
@@ -600,8 +643,12 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     g.out_ld = static_cast<int32_t>(K);
     g.out_valid = static_cast<int32_t>(K);
     g.out = dX;
-    dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(K, bn)), 1);
-    QL_TRY((launch_gemm<false, false>("gemm_dx", grid, tc, mdY, mWdT, mGs, mA, g, st)));
+    if (pair) {
+      QL_TRY(launch_gemm_pair("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, g, st));
+    } else {
+      dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(K, bn)), 1);
+      QL_TRY((launch_gemm<false, false>("gemm_dx", grid, tc, mdY, mWdT, mGs, mA, g, st)));
+    }
   }
 
   // 3. dA = s X^T G   (X read MN-major, split over M)
