@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "ptx.cuh"
+
 namespace qlora {
 
 // deq(W)[n,k] = bf16( fp32( codebook[code(n,k)] * absmax[(n*K+k)/64] ) ).
@@ -23,6 +25,8 @@ __global__ void __launch_bounds__(256) dequant4_kernel(const uint32_t* __restric
                                                        uint4* __restrict__ out_bf16,
                                                        float4* __restrict__ out_f32) {
   __shared__ float cb[16];
+  griddep_wait();
+  griddep_launch_dependents();
   if (threadIdx.x < 16) cb[threadIdx.x] = codebook[threadIdx.x];
   __syncthreads();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -64,6 +68,8 @@ __global__ void __launch_bounds__(256) dequant4_t_kernel(const uint8_t* __restri
                                                          __nv_bfloat16* __restrict__ outT, int64_t ldt) {
   __shared__ float cb[16];
   __shared__ __nv_bfloat16 tile[64][64 + 2];
+  griddep_wait();
+  griddep_launch_dependents();
   if (threadIdx.x < 16) cb[threadIdx.x] = codebook[threadIdx.x];
   __syncthreads();
   const int n0 = blockIdx.y * 64;
@@ -119,23 +125,43 @@ __global__ void __launch_bounds__(256) dequant4_t_kernel(const uint8_t* __restri
   }
 }
 
-// dst[c, rr] = src[rr, c] for rr < rows, c < cols; zero where dst_rows x
-// dst_cols extends beyond (padding).  Small operands only (rank-r sides).
-__global__ void transpose_pad_bf16_kernel(const __nv_bfloat16* __restrict__ src, int32_t rows, int32_t cols,
-                                          int64_t lds, __nv_bfloat16* __restrict__ dst, int32_t dst_rows,
-                                          int32_t dst_cols, int64_t ldd) {
-  __shared__ __nv_bfloat16 t[32][33];
-  const int r0 = blockIdx.x * 32;  // src rows = dst cols
-  const int c0 = blockIdx.y * 32;  // src cols = dst rows
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+// Up to three small transposes in one launch (blockIdx.z selects the job):
+// dst[c, rr] = src[rr, c] for rr < rows, c < cols, and zero where the
+// dst_rows x dst_cols destination extends beyond the source (padding).
+struct TransposeJob {
+  const __nv_bfloat16* src;
+  __nv_bfloat16* dst;
+  int32_t rows, cols, dst_rows, dst_cols;
+  int64_t lds, ldd;
+  int32_t tiles_x;      // 32-wide tiles over dst_cols
+  int32_t tile_begin;   // first flat tile index of this job
+};
+struct TransposeJobs {
+  TransposeJob job[3];
+  int32_t njobs;
+};
+
+// Flat grid: block b belongs to the last job whose tile_begin <= b.
+__global__ void __launch_bounds__(256) transpose_jobs_kernel(const TransposeJobs jobs) {
+  __shared__ __nv_bfloat16 t[32][34];
+  griddep_wait();
+  griddep_launch_dependents();
+  int j = 0;
+  for (int q = 1; q < jobs.njobs; ++q)
+    if (static_cast<int>(blockIdx.x) >= jobs.job[q].tile_begin) j = q;
+  const TransposeJob& jb = jobs.job[j];
+  const int local = static_cast<int>(blockIdx.x) - jb.tile_begin;
+  const int r0 = (local % jb.tiles_x) * 32;  // src rows = dst cols
+  const int c0 = (local / jb.tiles_x) * 32;  // src cols = dst rows
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   for (int i = ty; i < 32; i += 8) {
     const int rr = r0 + i, c = c0 + tx;
-    t[i][tx] = (rr < rows && c < cols) ? src[static_cast<int64_t>(rr) * lds + c] : __float2bfloat16_rn(0.f);
+    t[i][tx] = (rr < jb.rows && c < jb.cols) ? jb.src[static_cast<int64_t>(rr) * jb.lds + c] : __float2bfloat16_rn(0.f);
   }
   __syncthreads();
   for (int i = ty; i < 32; i += 8) {
     const int dr = c0 + i, dc = r0 + tx;
-    if (dr < dst_rows && dc < dst_cols) dst[static_cast<int64_t>(dr) * ldd + dc] = t[tx][i];
+    if (dr < jb.dst_rows && dc < jb.dst_cols) jb.dst[static_cast<int64_t>(dr) * jb.ldd + dc] = t[tx][i];
   }
 }
 
@@ -146,6 +172,8 @@ __global__ void transpose_pad_bf16_kernel(const __nv_bfloat16* __restrict__ src,
 //   out_bf16_t[j][i] = bf16(sum)            (ld_t)
 //   out_f32[i][j]    = scale * sum          (ld_o)
 //   out_f32_t[j][i]  = scale * sum          (ld_t)
+// One CTA reduces a 32 x 32 tile; the transposed outputs go through shared
+// memory so every global access is coalesced.
 struct ReduceArgs {
   const float* part;
   int32_t splits, rows, cols;
@@ -159,18 +187,36 @@ struct ReduceArgs {
   int64_t ld_o, ld_t;
 };
 
-__global__ void __launch_bounds__(256) reduce_splits_kernel(const ReduceArgs a) {
-  const int64_t total = static_cast<int64_t>(a.rows) * a.cols;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
-    const int64_t i = e / a.cols, j = e % a.cols;
+__global__ void __launch_bounds__(256) reduce_tile_kernel(const ReduceArgs a) {
+  __shared__ float t[32][33];
+  griddep_wait();
+  griddep_launch_dependents();
+  const int r0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int c = c0 + tx;
+  for (int i = ty; i < 32; i += 8) {
+    const int r = r0 + i;
     float acc = 0.f;
-    for (int s = 0; s < a.splits; ++s) acc += a.part[s * a.sstride + i * a.ld + j];
-    if (a.out_bf16) a.out_bf16[i * a.ld_o + j] = __float2bfloat16_rn(acc);
-    if (a.out_bf16_s) a.out_bf16_s[i * a.ld_o + j] = __float2bfloat16_rn(__fmul_rn(a.scale, acc));
-    if (a.out_bf16_t) a.out_bf16_t[j * a.ld_t + i] = __float2bfloat16_rn(acc);
-    if (a.out_f32) a.out_f32[i * a.ld_o + j] = __fmul_rn(a.scale, acc);
-    if (a.out_f32_t) a.out_f32_t[j * a.ld_t + i] = __fmul_rn(a.scale, acc);
+    if (r < a.rows && c < a.cols) {
+      const float* pp = a.part + static_cast<int64_t>(r) * a.ld + c;
+      for (int s = 0; s < a.splits; ++s) acc += pp[s * a.sstride];
+      const int64_t o = static_cast<int64_t>(r) * a.ld_o + c;
+      if (a.out_bf16) a.out_bf16[o] = __float2bfloat16_rn(acc);
+      if (a.out_bf16_s) a.out_bf16_s[o] = __float2bfloat16_rn(__fmul_rn(a.scale, acc));
+      if (a.out_f32) a.out_f32[o] = __fmul_rn(a.scale, acc);
+    }
+    t[i][tx] = acc;
+  }
+  if (!a.out_bf16_t && !a.out_f32_t) return;
+  __syncthreads();
+  for (int i = ty; i < 32; i += 8) {
+    const int cc = c0 + i, r = r0 + tx;
+    if (cc < a.cols && r < a.rows) {
+      const float v = t[tx][i];
+      const int64_t o = static_cast<int64_t>(cc) * a.ld_t + r;
+      if (a.out_bf16_t) a.out_bf16_t[o] = __float2bfloat16_rn(v);
+      if (a.out_f32_t) a.out_f32_t[o] = __fmul_rn(a.scale, v);
+    }
   }
 }
 

@@ -30,6 +30,9 @@ namespace qlora {
 
 constexpr uint32_t kPairStageBytes = 2 * 128 * 128;  // A half + B half, 64-wide K block
 
+// B_MN: B is read MN-major (its rows are reduction rows holding 64 output
+// columns each; used for dX straight from the row-major dequantised weight).
+template <bool B_MN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -86,6 +89,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_wait();  // the predecessor kernel's global writes are visible from here on
+  griddep_launch_dependents();
   const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);      // even CTA's ring barriers
   const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);  // even CTA's accumulator-empty
 
@@ -120,7 +125,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if (it < nkb) {
           const int kel = it * 64;
           tma_load_2d_pair_ws(a_dst, &tmA, bar, kel, m0);
-          tma_load_2d_pair_ws(b_dst, &tmB, bar, kel, n0);
+          if (B_MN) {
+            tma_load_2d_pair_ws(b_dst, &tmB, bar, n0, kel);
+            tma_load_2d_pair_ws(b_dst + 8192, &tmB, bar, n0 + 64, kel);
+          } else {
+            tma_load_2d_pair_ws(b_dst, &tmB, bar, kel, n0);
+          }
         } else {
           const int a = it - nkb;
           tma_load_2d_pair_ws(a_dst, &tmA2, bar, a2_x0 + 64 * a, m0);
@@ -137,7 +147,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer (even CTA; whole warp, elected lane issues) ----------------
     if (rank == 0) {
-      const uint32_t idesc = idesc_bf16_f32(256, 256, false, false);
+      const uint32_t idesc = idesc_bf16_f32(256, 256, false, B_MN);
+      const uint32_t idesc_lora = idesc_bf16_f32(256, 256, false, false);
       uint32_t g = 0;
       int j = 0;
       bool ok = true;
@@ -168,13 +179,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           const uint32_t a_addr = smem_u32(smem + s * kPairStageBytes);
           const uint32_t b_addr = a_addr + kATileBytes;
           if (it < nkb) {
-            tc_mma_bf16_pair_k64_ws(d_tmem, sdesc_sw128(a_addr, 16u, 1024u), sdesc_sw128(b_addr, 16u, 1024u), 2u, 2u,
+            const uint64_t bd = B_MN ? sdesc_sw128(b_addr, 8192u, 1024u) : sdesc_sw128(b_addr, 16u, 1024u);
+            tc_mma_bf16_pair_k64_ws(d_tmem, sdesc_sw128(a_addr, 16u, 1024u), bd, 2u, B_MN ? (2048u >> 4) : 2u,
                                     idesc, it > 0 ? 1u : 0u);
           } else {
             const int ksteps = min(4, p.lora_ksteps - 4 * (it - nkb));
             for (int kk = 0; kk < ksteps; ++kk)
               tc_mma_bf16_pair_ws(d_tmem, sdesc_sw128(a_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u),
-                                  sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u), idesc,
+                                  sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u), idesc_lora,
                                   (it > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit_pair_multicast_ws(&empty[s], 0x3);

@@ -193,6 +193,10 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above touched only on-chip state; global memory written by the
+  // predecessor kernel is visible after this point.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ---------------- TMA producer (whole warp, one elected lane issues) ----------------

@@ -388,3 +388,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 }
 
 }  // namespace qlora
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel may start while its predecessor in
+// the stream is finishing; griddep_wait() blocks until the predecessor grid
+// has completed and its memory is visible, griddep_launch_dependents() lets
+// the successor start launching.
+// ---------------------------------------------------------------------------
+namespace qlora {
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+}  // namespace qlora

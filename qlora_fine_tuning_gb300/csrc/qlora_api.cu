@@ -22,6 +22,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/qlora.h"
@@ -144,11 +145,14 @@ int splits_for_rows(int64_t nkb) {
 }
 
 int choose_splits(int64_t tiles, int64_t nkb) {
-  int64_t s = std::max<int64_t>(1, (kSMs + tiles / 2) / std::max<int64_t>(1, tiles));
+  int64_t s = std::max<int64_t>(1, kSMs / std::max<int64_t>(1, tiles));  // never more tiles than one wave
   s = std::min<int64_t>(s, kMaxSplits);
   s = std::min<int64_t>(s, std::max<int64_t>(1, nkb));
   return static_cast<int>(s);
 }
+
+// Workspace header: the device error word (first 4 bytes of 256).
+constexpr size_t kHeaderBytes = 256;
 
 struct Layout {
   int64_t M, N, K, r, nseg, R, Rp, Mp;
@@ -169,7 +173,7 @@ Layout layout(int64_t M, int64_t N, int64_t K, int64_t r, int64_t nseg) {
   L.Mp = rup(std::max<int64_t>(M, 1), 8);
   size_t o = 0;
   L.off_err = o;
-  o += 256;
+  o += kHeaderBytes;
   L.off_wd = o;
   o = align256(o + size_t(N) * K * 2);
   L.off_bt = o;
@@ -240,6 +244,33 @@ qlora_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QLORA_OK : Q
 // ---------------------------------------------------------------------------
 constexpr int kSmemLimit = 232448;
 
+// Every launch may overlap the tail of its predecessor in the stream
+// (programmatic dependent launch); each kernel waits (griddepcontrol.wait)
+// before it touches global memory.  QLORA_DISABLE_PDL=1 turns it off.
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("QLORA_DISABLE_PDL");
+    return !(e && e[0] == '1');
+  }();
+  return on;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 struct TileCfg {
   int bn, stages;
   uint32_t stage_bytes;
@@ -274,11 +305,12 @@ qlora_status launch_gemm(const char* name, dim3 grid, const TileCfg& tc, const C
   args.z_tiles = static_cast<int32_t>(grid.z);
   const int64_t tiles = int64_t(grid.x) * grid.y * grid.z;
   const unsigned ctas = static_cast<unsigned>(std::min<int64_t>(tiles, sm_count(dev)));
+  cudaError_t e;
   {
     LaunchScope ls(name, st);
-    gemm_tc_kernel<A_MN, F32><<<ctas, 192, tc.smem, st>>>(a, b, a2, b2, args);
+    e = launch_k(gemm_tc_kernel<A_MN, F32>, dim3(ctas), dim3(192), tc.smem, st, a, b, a2, b2, args);
   }
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
 // CTA-pair kernel for the two large GEMMs (256 x 256 tiles, K-major operands).
@@ -289,6 +321,7 @@ bool pair_enabled() {
   return !(e && e[0] == '1');
 }
 
+template <bool B_MN>
 qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles, const CUtensorMap& a,
                               const CUtensorMap& b, const CUtensorMap& a2, const CUtensorMap& b2, GemmArgs args,
                               cudaStream_t st) {
@@ -297,7 +330,7 @@ qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles
   cudaGetDevice(&dev);
   const size_t smem = size_t(kPairStages) * kPairStageBytes + 1024 + 256;
   std::call_once(attr_once[dev & 63], [smem] {
-    cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaFuncSetAttribute(gemm_pair_kernel<B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   });
   args.bn = 256;
   args.stages = kPairStages;
@@ -307,13 +340,17 @@ qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles
   args.n_tiles = static_cast<int32_t>(n_tiles);
   args.z_tiles = 1;
   const int64_t pairs = std::min<int64_t>(m_tiles * n_tiles, sm_count(dev) / 2);
+  cudaError_t e;
   {
     LaunchScope ls(name, st);
-    gemm_pair_kernel<<<static_cast<unsigned>(2 * pairs), 192, smem, st>>>(a, b, a2, b2, args);
+    e = launch_k(gemm_pair_kernel<B_MN>, dim3(static_cast<unsigned>(2 * pairs)), dim3(192), smem, st, a, b, a2, b2,
+                 args);
   }
-  return cuda_status(cudaGetLastError());
+  return cuda_status(e);
 }
 
+// Let the kernel finish its split reduction when there are counters for all
+// of its output tiles; otherwise the caller runs reduce_tile_kernel.
 GemmArgs base_args(uint32_t* err) {
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
@@ -328,29 +365,47 @@ qlora_status launch_dequant(const qlora_w4* w, void* out_bf16, float* out_f32, c
   if (groups == 0) return QLORA_OK;
   const int64_t blocks = std::min<int64_t>(cdiv(groups, 256), int64_t(kSMs) * 16);
   LaunchScope ls("dequant4", st);
-  dequant4_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-      reinterpret_cast<const uint32_t*>(w->idx), w->absmax, w->codebook, groups, reinterpret_cast<uint4*>(out_bf16),
-      reinterpret_cast<float4*>(out_f32));
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(dequant4_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                              reinterpret_cast<const uint32_t*>(w->idx), w->absmax, w->codebook, groups,
+                              reinterpret_cast<uint4*>(out_bf16), reinterpret_cast<float4*>(out_f32)));
 }
 
-qlora_status launch_transpose(const char* name, const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst,
-                              int64_t drows, int64_t dcols, int64_t ldd, cudaStream_t st) {
-  dim3 grid(static_cast<unsigned>(cdiv(dcols, 32)), static_cast<unsigned>(cdiv(drows, 32)));
+TransposeJob tjob(const void* src, int64_t rows, int64_t cols, int64_t lds, void* dst, int64_t drows, int64_t dcols,
+                  int64_t ldd) {
+  TransposeJob j;
+  j.src = reinterpret_cast<const __nv_bfloat16*>(src);
+  j.dst = reinterpret_cast<__nv_bfloat16*>(dst);
+  j.rows = static_cast<int32_t>(rows);
+  j.cols = static_cast<int32_t>(cols);
+  j.dst_rows = static_cast<int32_t>(drows);
+  j.dst_cols = static_cast<int32_t>(dcols);
+  j.lds = lds;
+  j.ldd = ldd;
+  return j;
+}
+
+// One launch for up to three transposes (tiles of all jobs in one flat grid).
+qlora_status launch_transposes(const char* name, const TransposeJob* jobs, int n, cudaStream_t st) {
+  TransposeJobs tj;
+  std::memset(&tj, 0, sizeof(tj));
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    tj.job[i] = jobs[i];
+    tj.job[i].tiles_x = static_cast<int32_t>(cdiv(jobs[i].dst_cols, 32));
+    tj.job[i].tile_begin = static_cast<int32_t>(total);
+    total += cdiv(jobs[i].dst_cols, 32) * cdiv(jobs[i].dst_rows, 32);
+  }
+  tj.njobs = n;
+  if (total == 0) return QLORA_OK;
   LaunchScope ls(name, st);
-  transpose_pad_bf16_kernel<<<grid, 256, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(src), static_cast<int32_t>(rows), static_cast<int32_t>(cols), lds,
-      reinterpret_cast<__nv_bfloat16*>(dst), static_cast<int32_t>(drows), static_cast<int32_t>(dcols), ldd);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(transpose_jobs_kernel, dim3(static_cast<unsigned>(total)), dim3(256), 0, st, tj));
 }
 
 qlora_status launch_reduce(const char* name, const ReduceArgs& ra, cudaStream_t st) {
-  const int64_t total = int64_t(ra.rows) * ra.cols;
-  if (total == 0) return QLORA_OK;
-  const int64_t blocks = std::min<int64_t>(cdiv(total, 256), int64_t(kSMs) * 8);
+  if (int64_t(ra.rows) * ra.cols == 0) return QLORA_OK;
+  dim3 grid(static_cast<unsigned>(cdiv(ra.rows, 32)), static_cast<unsigned>(cdiv(ra.cols, 32)));
   LaunchScope ls(name, st);
-  reduce_splits_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(ra);
-  return cuda_status(cudaGetLastError());
+  return cuda_status(launch_k(reduce_tile_kernel, grid, dim3(256), 0, st, ra));
 }
 
 ReduceArgs reduce_args(const float* part, int splits, int64_t rows, int64_t cols, int64_t ld, int64_t sstride,
@@ -485,8 +540,10 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
   // 1. Wd = deq(W)
   QL_TRY(launch_dequant(W, Wd, nullptr, st));
   // 2. A^T [R,K], B^T [N,Rp] (zero columns r..Rp-1)
-  QL_TRY(launch_transpose("transpose_A", A, K, R, R, At, R, K, K, st));
-  QL_TRY(launch_transpose("transpose_B", B, r, N, N, Bt, N, L.Rp, L.Rp, st));
+  {
+    const TransposeJob jobs[2] = {tjob(A, K, R, R, At, R, K, K), tjob(B, r, N, N, Bt, N, L.Rp, L.Rp)};
+    QL_TRY(launch_transposes("transpose_AB", jobs, 2, st));
+  }
 
   // 3. XA = X . A  (split over K)
   CUtensorMap mX, mAt, mWd, mXAs, mBt;
@@ -509,11 +566,13 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     g.out = part;
     QL_TRY((launch_gemm<false, true>("gemm_xa", dim3(static_cast<unsigned>(mt), 1, splits), tc, mX, mAt, mX, mAt, g,
                                      st)));
-    ReduceArgs ra = reduce_args(part, splits, M, R, R, M * R, s);
-    ra.out_bf16 = reinterpret_cast<__nv_bfloat16*>(XA_save);
-    ra.out_bf16_s = reinterpret_cast<__nv_bfloat16*>(XAs);
-    ra.ld_o = R;
-    QL_TRY(launch_reduce("reduce_xa", ra, st));
+    {
+      ReduceArgs ra = reduce_args(part, splits, M, R, R, M * R, s);
+      ra.out_bf16 = reinterpret_cast<__nv_bfloat16*>(XA_save);
+      ra.out_bf16_s = reinterpret_cast<__nv_bfloat16*>(XAs);
+      ra.ld_o = R;
+      QL_TRY(launch_reduce("reduce_xa", ra, st));
+    }
   }
 
   // 4. Y = X . Wd^T + (s XA) . B
@@ -542,7 +601,7 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     g.out_valid = static_cast<int32_t>(N);
     g.out = Y;
     if (pair) {
-      QL_TRY(launch_gemm_pair("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, g, st));
+      QL_TRY(launch_gemm_pair<false>("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, g, st));
     } else {
       dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(N, bn)), 1);
       QL_TRY((launch_gemm<false, false>("gemm_fwd", grid, tc, mX, mWd, mXAs, mBt, g, st)));
@@ -607,30 +666,37 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     g.out = part;
     QL_TRY((launch_gemm<false, true>("gemm_g", dim3(static_cast<unsigned>(mt), 1, splits * n_seg), tc, mdY, mB, mdY,
                                      mB, g, st)));
-    ReduceArgs ra = reduce_args(part, splits, M, R, R, M * R, s);
-    ra.out_bf16_s = reinterpret_cast<__nv_bfloat16*>(Gs);
-    ra.out_bf16_t = reinterpret_cast<__nv_bfloat16*>(Gt);
-    ra.ld_o = R;
-    ra.ld_t = L.Mp;
-    QL_TRY(launch_reduce("reduce_g", ra, st));
+    {
+      ReduceArgs ra = reduce_args(part, splits, M, R, R, M * R, s);
+      ra.out_bf16_s = reinterpret_cast<__nv_bfloat16*>(Gs);
+      ra.out_bf16_t = reinterpret_cast<__nv_bfloat16*>(Gt);
+      ra.ld_o = R;
+      ra.ld_t = L.Mp;
+      QL_TRY(launch_reduce("reduce_g", ra, st));
+    }
   }
 
   // 2. dX = dY . Wd + (s G) . A^T
   if (dX) {
-    {
-      dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(cdiv(N, 64)));
-      LaunchScope ls("dequant4_t", st);
-      dequant4_t_kernel<<<grid, 256, 0, st>>>(W->idx, W->absmax, W->codebook, static_cast<int32_t>(N),
-                                              static_cast<int32_t>(K), reinterpret_cast<__nv_bfloat16*>(WdT), N);
-      QL_TRY(cuda_status(cudaGetLastError()));
-    }
+    const bool pair = pair_enabled();
     const int bn = 256;
     const TileCfg tc = tile_cfg(bn);
-    const bool pair = pair_enabled();
+    if (pair) {
+      // row-major Wd [N,K], read MN-major by the pair kernel
+      QL_TRY(launch_dequant(W, WdT, nullptr, st));
+      if (!make_map(&mWdT, WdT, K, N, K, 64)) return QLORA_ERR_CUDA;
+    } else {
+      dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(cdiv(N, 64)));
+      {
+        LaunchScope ls("dequant4_t", st);
+        QL_TRY(cuda_status(launch_k(dequant4_t_kernel, grid, dim3(256), 0, st, W->idx, W->absmax, W->codebook,
+                                    static_cast<int32_t>(N), static_cast<int32_t>(K),
+                                    reinterpret_cast<__nv_bfloat16*>(WdT), N)));
+      }
+      if (!make_map(&mWdT, WdT, N, K, N, static_cast<uint32_t>(bn))) return QLORA_ERR_CUDA;
+    }
     const uint32_t brows = pair ? 128u : static_cast<uint32_t>(bn);
-    if (!make_map(&mWdT, WdT, N, K, N, brows) || !make_map(&mGs, Gs, R, M, R, 128) ||
-        !make_map(&mA, A, R, K, R, brows))
-      return QLORA_ERR_CUDA;
+    if (!make_map(&mGs, Gs, R, M, R, 128) || !make_map(&mA, A, R, K, R, brows)) return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(M);
     g.N = static_cast<int32_t>(K);
@@ -644,7 +710,7 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     g.out_valid = static_cast<int32_t>(K);
     g.out = dX;
     if (pair) {
-      QL_TRY(launch_gemm_pair("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, g, st));
+      QL_TRY(launch_gemm_pair<true>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, g, st));
     } else {
       dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(K, bn)), 1);
       QL_TRY((launch_gemm<false, false>("gemm_dx", grid, tc, mdY, mWdT, mGs, mA, g, st)));
@@ -671,15 +737,20 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     g.out = part;
     QL_TRY((launch_gemm<true, true>("gemm_da", dim3(static_cast<unsigned>(kt), 1, splits), tc, mXmn, mGt, mXmn, mGt,
                                     g, st)));
-    ReduceArgs ra = reduce_args(part, splits, K, R, R, K * R, s);
-    ra.out_f32 = dA;
-    ra.ld_o = R;
-    QL_TRY(launch_reduce("reduce_da", ra, st));
+    {
+      ReduceArgs ra = reduce_args(part, splits, K, R, R, K * R, s);
+      ra.out_f32 = dA;
+      ra.ld_o = R;
+      QL_TRY(launch_reduce("reduce_da", ra, st));
+    }
   }
 
   // 4. dB = s XA^T dY  (computed as dB^T = dY^T . XA with dY read MN-major)
   {
-    QL_TRY(launch_transpose("transpose_XA", XA_saved, M, R, R, XAt, R, L.Mp, L.Mp, st));
+    {
+      const TransposeJob jobs[1] = {tjob(XA_saved, M, R, R, XAt, R, L.Mp, L.Mp)};
+      QL_TRY(launch_transposes("transpose_XA", jobs, 1, st));
+    }
     const int bn = static_cast<int>(rup(r, 16));
     const TileCfg tc = tile_cfg(bn);
     const int64_t nt = cdiv(N, 128);
@@ -701,10 +772,12 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     g.out = part;
     QL_TRY((launch_gemm<true, true>("gemm_db", dim3(static_cast<unsigned>(nt), 1, splits), tc, mdYmn, mXAt, mdYmn,
                                     mXAt, g, st)));
-    ReduceArgs ra = reduce_args(part, splits, N, r, r, N * r, s);
-    ra.out_f32_t = dB;
-    ra.ld_t = N;
-    QL_TRY(launch_reduce("reduce_db", ra, st));
+    {
+      ReduceArgs ra = reduce_args(part, splits, N, r, r, N * r, s);
+      ra.out_f32_t = dB;
+      ra.ld_t = N;
+      QL_TRY(launch_reduce("reduce_db", ra, st));
+    }
   }
   return QLORA_OK;
 }
@@ -760,7 +833,10 @@ extern "C" qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t
   void* At = b8;
   float* part = reinterpret_cast<float*>(b8 + at_bytes);
 
-  QL_TRY(launch_transpose("transpose_A_static", A, K, R, R, At, R, K, K, st));
+  {
+    const TransposeJob jobs[1] = {tjob(A, K, R, R, At, R, K, K)};
+    QL_TRY(launch_transposes("transpose_A_static", jobs, 1, st));
+  }
   const int bn = static_cast<int>(rup(R, 16));
   const TileCfg tc = tile_cfg(bn);
   CUtensorMap mAt;
