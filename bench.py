@@ -286,45 +286,90 @@ def run_ours(args, rank, world):
                  for name, n, ms in kstats}
 
     # ---- end to end: pinned host inputs -> device, result gradients back ----
+    # Host-to-device copies of the next inputs overlap compute (a copy stream
+    # and two alternating sets of device input buffers), as in the pages'
+    # double-buffered asynchronous reload; dA / dB go back on a third stream.
     e2e = None
     if not args.no_e2e:
+        nl = len(layers)
         hX = [torch.from_numpy(np.ascontiguousarray(L["li"].X).view(np.int16)).view(torch.bfloat16).pin_memory()
               for L in layers]
         hdY = [torch.from_numpy(np.ascontiguousarray(L["li"].dY).view(np.int16)).view(torch.bfloat16).pin_memory()
                for L in layers]
-        dX_in = [torch.empty_like(L["X"]) for L in layers]
-        ddY_in = [torch.empty_like(L["dY"]) for L in layers]
+        bufX = [[torch.empty_like(L["X"]) for L in layers] for _ in range(2)]
+        bufdY = [[torch.empty_like(L["dY"]) for L in layers] for _ in range(2)]
         hdA = [torch.empty(L["dA"].shape, dtype=torch.float32).pin_memory() for L in layers]
         hdB = [torch.empty(L["dB"].shape, dtype=torch.float32).pin_memory() for L in layers]
         h2d = sum(t.numel() * 2 for t in hX) + sum(t.numel() * 2 for t in hdY)
         d2h = sum(t.numel() * 4 for t in hdA) + sum(t.numel() * 4 for t in hdB)
+        up = torch.cuda.Stream()
+        down = torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        ev_x = [[ev() for _ in range(nl)] for _ in range(2)]
+        ev_dy = [[ev() for _ in range(nl)] for _ in range(2)]
+        ev_free = [[None] * nl for _ in range(2)]   # compute finished with buffer set b, linear i
+        ev_bwd = [ev() for _ in range(nl)]
+        ev_back = [None] * nl                        # dA/dB of linear i copied back
 
-        def e2e_step():
-            for i in range(len(layers)):
-                dX_in[i].copy_(hX[i], non_blocking=True)
-                ddY_in[i].copy_(hdY[i], non_blocking=True)
-            step(dX_in, ddY_in)
+        def e2e_step(sidx):
+            b = sidx % 2
+            with torch.cuda.stream(up):
+                for i in range(nl):
+                    if ev_free[b][i] is not None:
+                        up.wait_event(ev_free[b][i])
+                    bufX[b][i].copy_(hX[i], non_blocking=True)
+                    ev_x[b][i].record(up)
+                for i in reversed(range(nl)):
+                    bufdY[b][i].copy_(hdY[i], non_blocking=True)
+                    ev_dy[b][i].record(up)
             for i, L in enumerate(layers):
-                hdA[i].copy_(L["dA"], non_blocking=True)
-                hdB[i].copy_(L["dB"], non_blocking=True)
+                li = L["li"]
+                stream.wait_event(ev_x[b][i])
+                binding.qlora_linear_fwd(bufX[b][i], li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["Y"],
+                                         L["XA"], ws, ws_bytes, stream)
+            for i in reversed(range(nl)):
+                L = layers[i]
+                li = L["li"]
+                stream.wait_event(ev_dy[b][i])
+                if ev_back[i] is not None:
+                    stream.wait_event(ev_back[i])   # previous dA/dB of this linear copied out
+                binding.qlora_linear_bwd(bufdY[b][i], bufX[b][i], L["XA"], li.M, L["w"], L["A"], L["B"], li.r,
+                                         L["seg"], li.s, L["dX"], L["dA"], L["dB"], ws, ws_bytes, stream)
+                ev_bwd[i].record(stream)
+                fr = ev()
+                fr.record(stream)
+                ev_free[b][i] = fr
+                with torch.cuda.stream(down):
+                    down.wait_event(ev_bwd[i])
+                    hdA[i].copy_(L["dA"], non_blocking=True)
+                    hdB[i].copy_(L["dB"], non_blocking=True)
+                    bk = ev()
+                    bk.record(down)
+                    ev_back[i] = bk
 
-        for _ in range(2):
-            e2e_step()
+        for w_ in range(2):
+            e2e_step(w_)
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(up)
+        stream.wait_event(e0)
+        down.wait_event(e0)
+        for k in range(args.steps):
+            e2e_step(k)
+        done_c = ev()
+        done_c.record(stream)
+        down.wait_event(done_c)
+        down.wait_event(up.record_event())
+        e1.record(down)
         torch.cuda.synchronize()
         barrier(world)
         ems = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
         e2e = {"value": round(flops * world / (ems * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(ems, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "what": "per step: X and dY of every linear copied from pinned host memory, fwd+bwd through "
-                       "the C ABI, dA and dB copied back"}
+               "what": "per step: X and dY of every linear copied from pinned host memory (copy stream, "
+                       "double-buffered, overlapping compute), fwd+bwd through the C ABI, dA and dB copied back"}
         st = binding.qlora_check_device_error(ws)
         if st != binding.OK:
             raise RuntimeError(f"device error in e2e region: {binding.STATUS[st]}")

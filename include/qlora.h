@@ -119,6 +119,15 @@ qlora_status qlora_check_device_error(void* ws, cudaStream_t stream);
  * (default 2e9).  Values below 1e6 are raised to 1e6. */
 void qlora_set_wait_limit_ns(uint64_t ns);
 
+/* Test hook for the failure path: the next launch of the GEMM with this label
+ * ("gemm_xa", "gemm_fwd", "gemm_g", "gemm_dx", "gemm_da" or "gemm_db")
+ * leaves the first shared-memory stage of its first CTA (CTA pair) unfilled,
+ * so that CTA's consumer wait runs out after the wait limit; the kernel then
+ * winds down, frees its tensor memory and sets the workspace error flag, and
+ * qlora_check_device_error returns QLORA_ERR_TIMEOUT.  That call's outputs
+ * are not valid; later calls work normally.  NULL clears a pending request. */
+void qlora_debug_stall_next_launch(const char* label);
+
 /* Human-readable name of a status code (static storage). */
 const char* qlora_status_str(qlora_status status);
 

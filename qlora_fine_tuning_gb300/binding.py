@@ -87,6 +87,8 @@ def lib(path: Optional[str] = None):
             L.qlora_profiler_collect.argtypes = [ctypes.POINTER(KernelStat), ctypes.c_int]
             L.qlora_launch_counter.restype = ctypes.c_uint64
             L.qlora_launch_counter.argtypes = []
+            L.qlora_debug_stall_next_launch.restype = None
+            L.qlora_debug_stall_next_launch.argtypes = [ctypes.c_char_p]
             L.qlora_linear_xa_static.restype = ctypes.c_int
             L.qlora_linear_xa_static.argtypes = [P, I64, I64, P, I32, P, P]
             _lib = L
@@ -174,6 +176,10 @@ def qlora_check_device_error(ws, stream=None) -> int:
 
 def qlora_set_wait_limit_ns(ns: int) -> None:
     lib().qlora_set_wait_limit_ns(int(ns))
+
+
+def qlora_debug_stall_next_launch(label) -> None:
+    lib().qlora_debug_stall_next_launch(None if label is None else label.encode())
 
 
 def qlora_status_str(status: int) -> str:

@@ -118,6 +118,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           ok = false;
           break;
         }
+        if (p.debug_stall && g == 0 && pair == 0 && rank == 0) {  // even CTA never arms stage 0
+          ++g;
+          continue;
+        }
         uint8_t* a_dst = smem + s * kPairStageBytes;
         uint8_t* b_dst = a_dst + kATileBytes;
         const uint32_t bar = full0 + s * 8u;

@@ -71,6 +71,7 @@ struct GemmArgs {
   void* out;
   uint32_t* err;        // device error word (bit flags), may be null
   uint64_t timeout_ns;  // bound on every barrier wait
+  int32_t debug_stall;  // test hook: CTA (pair) 0 never fills its first stage
 };
 
 struct TileInfo {
@@ -215,6 +216,10 @@ __global__ void __launch_bounds__(192, 1)
           }
           ok = false;
           break;
+        }
+        if (p.debug_stall && g == 0 && blockIdx.x == 0) {  // leave stage 0 empty: its consumer times out
+          ++g;
+          continue;
         }
         uint8_t* a_dst = smem + s * p.stage_bytes;
         uint8_t* b_dst = a_dst + kATileBytes;

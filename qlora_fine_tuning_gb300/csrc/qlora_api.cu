@@ -38,6 +38,17 @@ namespace {
 // Settings, profiler
 // ---------------------------------------------------------------------------
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+// Test hook: label of the next GEMM launch that must stall (empty = none).
+std::mutex g_stall_mu;
+char g_stall_label[32] = {0};
+
+bool take_stall(const char* name) {
+  std::lock_guard<std::mutex> lk(g_stall_mu);
+  if (g_stall_label[0] == 0 || std::strcmp(g_stall_label, name) != 0) return false;
+  g_stall_label[0] = 0;
+  return true;
+}
 std::atomic<uint64_t> g_launches{0};
 
 struct ProfRec {
@@ -299,6 +310,7 @@ qlora_status launch_gemm(const char* name, dim3 grid, const TileCfg& tc, const C
   args.stages = tc.stages;
   args.stage_bytes = tc.stage_bytes;
   args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  args.debug_stall = take_stall(name) ? 1 : 0;
   // `grid` is the tile grid; the kernel is persistent with one CTA per SM.
   args.m_tiles = static_cast<int32_t>(grid.x);
   args.n_tiles = static_cast<int32_t>(grid.y);
@@ -336,6 +348,7 @@ qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles
   args.stages = kPairStages;
   args.stage_bytes = kPairStageBytes;
   args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  args.debug_stall = take_stall(name) ? 1 : 0;
   args.m_tiles = static_cast<int32_t>(m_tiles);
   args.n_tiles = static_cast<int32_t>(n_tiles);
   args.z_tiles = 1;
@@ -449,6 +462,15 @@ const char* qlora_status_str(qlora_status s) {
 }
 
 void qlora_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(std::max<uint64_t>(ns, 1000000ull)); }
+
+void qlora_debug_stall_next_launch(const char* label) {
+  std::lock_guard<std::mutex> lk(g_stall_mu);
+  g_stall_label[0] = 0;
+  if (label) {
+    std::strncpy(g_stall_label, label, sizeof(g_stall_label) - 1);
+    g_stall_label[sizeof(g_stall_label) - 1] = 0;
+  }
+}
 
 void qlora_profiler_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
