@@ -43,6 +43,7 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="launch every step instead of replaying a CUDA graph")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     return p.parse_args()
@@ -198,18 +199,19 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
 
     def step(Xs=None, dYs=None):
+        cur = torch.cuda.current_stream()  # the capture stream while a graph is recorded
         for i, L in enumerate(layers):
             li = L["li"]
             X = L["X"] if Xs is None else Xs[i]
             binding.qlora_linear_fwd(X, li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["Y"], L["XA"], ws,
-                                     ws_bytes, stream)
+                                     ws_bytes, cur)
         for i in reversed(range(len(layers))):
             L = layers[i]
             li = L["li"]
             X = L["X"] if Xs is None else Xs[i]
             dY = L["dY"] if dYs is None else dYs[i]
             binding.qlora_linear_bwd(dY, X, L["XA"], li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["dX"],
-                                     L["dA"], L["dB"], ws, ws_bytes, stream)
+                                     L["dA"], L["dB"], ws, ws_bytes, cur)
 
     for _ in range(args.warmup):
         step()
@@ -217,6 +219,21 @@ def run_ours(args, rank, world):
     st = binding.qlora_check_device_error(ws)
     if st != binding.OK:
         raise RuntimeError(f"device error after warm-up: {binding.STATUS[st]}")
+
+    # One step recorded as a CUDA graph (the library's launches are plain
+    # stream launches, so they capture as they are); replaying it removes the
+    # host launch path from the timed region.
+    graph = None
+    per_step_launches = None
+    if not args.no_graph:
+        c0 = binding.qlora_launch_counter()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        per_step_launches = binding.qlora_launch_counter() - c0
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
 
     # ---- timed region: device-resident inputs ----
     clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
@@ -229,11 +246,16 @@ def run_ours(args, rank, world):
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     launches = binding.qlora_launch_counter() - launches0
+    if graph is not None:
+        launches = per_step_launches * args.steps
     ms_total = ev0.elapsed_time(ev1)
     clk = clocks.stop()
     # ---- the same steps again with CUDA events around every library launch ----
@@ -393,6 +415,7 @@ def run_ours(args, rank, world):
         "roofline": roofline,
         "kernels": breakdown,
         "gpu_launches": int(launches),
+        "cuda_graph": graph is not None,
         "clocks": clk,
         "e2e": e2e,
     }

@@ -97,6 +97,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs; whole warp, elected lane issues) ----------------
     const uint32_t tx_pair = 2u * kPairStageBytes;
+    const uint64_t pol_a = (p.l2_hints & 2) ? l2_policy_evict_last() : l2_policy_evict_normal();
+    const uint64_t pol_b = (p.l2_hints & 4) ? l2_policy_evict_first() : l2_policy_evict_normal();
     uint32_t g = 0;
     bool ok = true;
     for (int tile = pair; tile < total && ok; tile += npairs) {
@@ -128,12 +130,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         if (rank == 0) mbar_arrive_expect_tx_ws(&full[s], tx_pair);
         if (it < nkb) {
           const int kel = it * 64;
-          tma_load_2d_pair_ws(a_dst, &tmA, bar, kel, m0);
+          tma_load_2d_pair_hint_ws(a_dst, &tmA, bar, kel, m0, pol_a);
           if (B_MN) {
-            tma_load_2d_pair_ws(b_dst, &tmB, bar, n0, kel);
-            tma_load_2d_pair_ws(b_dst + 8192, &tmB, bar, n0 + 64, kel);
+            tma_load_2d_pair_hint_ws(b_dst, &tmB, bar, n0, kel, pol_b);
+            tma_load_2d_pair_hint_ws(b_dst + 8192, &tmB, bar, n0 + 64, kel, pol_b);
           } else {
-            tma_load_2d_pair_ws(b_dst, &tmB, bar, kel, n0);
+            tma_load_2d_pair_hint_ws(b_dst, &tmB, bar, kel, n0, pol_b);
           }
         } else {
           const int a = it - nkb;
@@ -236,7 +238,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             w.y = pack_bf16x2(__uint_as_float(v[gq * 8 + 2]), __uint_as_float(v[gq * 8 + 3]));
             w.z = pack_bf16x2(__uint_as_float(v[gq * 8 + 4]), __uint_as_float(v[gq * 8 + 5]));
             w.w = pack_bf16x2(__uint_as_float(v[gq * 8 + 6]), __uint_as_float(v[gq * 8 + 7]));
-            *reinterpret_cast<uint4*>(out + col) = w;
+            if (p.l2_hints & 1) __stcs(reinterpret_cast<uint4*>(out + col), w);
+            else *reinterpret_cast<uint4*>(out + col) = w;
           }
         }
       }

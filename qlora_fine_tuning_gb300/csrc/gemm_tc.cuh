@@ -72,6 +72,8 @@ struct GemmArgs {
   uint32_t* err;        // device error word (bit flags), may be null
   uint64_t timeout_ns;  // bound on every barrier wait
   int32_t debug_stall;  // test hook: CTA (pair) 0 never fills its first stage
+  int32_t l2_hints;     // bit 0: streaming (evict-first) output stores;
+                        // bit 1: A loads evict-last; bit 2: B loads evict-first
 };
 
 struct TileInfo {
@@ -352,7 +354,8 @@ __global__ void __launch_bounds__(192, 1)
               w.y = pack_bf16x2(__uint_as_float(v[gq * 8 + 2]), __uint_as_float(v[gq * 8 + 3]));
               w.z = pack_bf16x2(__uint_as_float(v[gq * 8 + 4]), __uint_as_float(v[gq * 8 + 5]));
               w.w = pack_bf16x2(__uint_as_float(v[gq * 8 + 6]), __uint_as_float(v[gq * 8 + 7]));
-              *reinterpret_cast<uint4*>(out + col) = w;
+              if (p.l2_hints & 1) __stcs(reinterpret_cast<uint4*>(out + col), w);
+              else *reinterpret_cast<uint4*>(out + col) = w;
             }
           }
         }
