@@ -19,6 +19,22 @@
 //   warps 2..5     epilogue for this CTA's 128 rows; release the accumulator
 //                  by arriving on the even CTA's "accumulator empty" barrier.
 // Two TMEM accumulators of 256 columns (512 columns, allocated for the pair).
+//
+// FUSED_DQ: the B operand is the frozen 4-bit weight itself.  Per stage the
+// producer brings this CTA's packed codes and absmax in by TMA into a staging
+// area; 8 more warps (6..13) expand them -- fp32 product codebook * absmax,
+// round-to-nearest-even to bf16, exactly as dequant_4bit -- straight into the
+// 128-byte-swizzled B tile (K-major for Y, MN-major for dX), make the writes
+// visible to the tensor core (fence.proxy.async) and arrive on the even CTA's
+// "full" barrier next to the TMA bytes of A.  No dequantised copy of W is
+// ever written to memory.
+//
+// Measured on GB300 this variant is ~3x slower than dequantising W once per
+// call with dequant4_kernel and feeding bf16 tiles by TMA: the expansion adds
+// several hand-offs (staging TMA, dequant-warp wake-up, proxy fence,
+// cross-CTA arrival) to every stage's turnaround, which the 5-stage ring
+// (38 KiB stages) cannot hide.  The library therefore runs it only on request
+// (QLORA_FUSED_DQ=1).
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -29,25 +45,54 @@
 namespace qlora {
 
 constexpr uint32_t kPairStageBytes = 2 * 128 * 128;  // A half + B half, 64-wide K block
+constexpr uint32_t kRawBytes = 4096 + 2048;           // packed codes + absmax box
+constexpr uint32_t kPairDqStageBytes = 38912;         // A + B + raw, rounded to 1 KiB
+constexpr int kDqWarps = 8;
+
+// One dequant thread expands 32 codes (16 packed bytes) of one smem row into
+// four swizzled 16-byte chunks of bf16: chunk `c0 + c` of row `row` of the
+// 64-wide block at `blk`.
+__device__ __forceinline__ void dq_row32(const uint8_t* packed16, float am, const float* cb, uint8_t* blk, int row,
+                                         int c0) {
+  const uint4 pk = *reinterpret_cast<const uint4*>(packed16);
+  const uint32_t words[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t byte = (words[c] >> (8 * b)) & 0xFFu;
+      o[b] = pack_bf16x2(__fmul_rn(cb[byte & 0xFu], am), __fmul_rn(cb[byte >> 4], am));
+    }
+    const int chunk = (c0 + c) ^ (row & 7);
+    *reinterpret_cast<uint4*>(blk + row * 128 + chunk * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
 
 // B_MN: B is read MN-major (its rows are reduction rows holding 64 output
 // columns each; used for dX straight from the row-major dequantised weight).
-template <bool B_MN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+// With FUSED_DQ, tmB maps the packed codes (uint8 [N, K/2]) and tmS the
+// absmax (fp32 [N, K/64]); otherwise tmB maps the bf16 B operand and tmS is
+// unused.
+template <bool B_MN, bool FUSED_DQ>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-                     const GemmArgs p) {
+                     const __grid_constant__ CUtensorMap tmS, const GemmArgs p) {
+  constexpr uint32_t kStage = FUSED_DQ ? kPairDqStageBytes : kPairStageBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((((raw + 1023u) & ~1023u)) - raw);
-  uint8_t* ctrl = smem + static_cast<uint32_t>(p.stages) * kPairStageBytes;
+  uint8_t* ctrl = smem + static_cast<uint32_t>(p.stages) * kStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* raw_full = mma_done + 1;  // [kMaxStages] packed codes + absmax landed (FUSED_DQ)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_full + kMaxStages);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  float* cb_s = reinterpret_cast<float*>(tmem_slot + 4);  // [16] codebook (FUSED_DQ)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -62,8 +107,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.stages; ++i) {
-      mbar_init(&full[i], 1);
+      // TMA arrival of the even CTA, plus every dequant warp of both CTAs
+      mbar_init(&full[i], FUSED_DQ ? 1 + 2 * kDqWarps : 1);
       mbar_init(&empty[i], 1);
+      mbar_init(&raw_full[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -91,15 +138,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();  // the predecessor kernel's global writes are visible from here on
   griddep_launch_dependents();
+  if (FUSED_DQ && threadIdx.x < 16) cb_s[threadIdx.x] = p.codebook[threadIdx.x];
+  if (FUSED_DQ) __syncthreads();
   const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);      // even CTA's ring barriers
   const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);  // even CTA's accumulator-empty
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs; whole warp, elected lane issues) ----------------
     const uint32_t tx_pair = 2u * kPairStageBytes;
+    const uint32_t tx_a_pair = 2u * kATileBytes;
+    const uint32_t tx_raw = B_MN ? 4096u + 1024u : 4096u + 2048u;
     const uint64_t pol_a = (p.l2_hints & 2) ? l2_policy_evict_last() : l2_policy_evict_normal();
     const uint64_t pol_b = (p.l2_hints & 4) ? l2_policy_evict_first() : l2_policy_evict_normal();
     uint32_t g = 0;
+    uint32_t raw_issued = 0;  // bit i: ring position g-1-i had a packed-code load in flight
     bool ok = true;
     for (int tile = pair; tile < total && ok; tile += npairs) {
       const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
@@ -120,13 +172,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
           ok = false;
           break;
         }
-        if (p.debug_stall && g == 0 && pair == 0 && rank == 0) {  // even CTA never arms stage 0
+        raw_issued <<= 1;
+        // Test hook: the even CTA of pair 0 never arms stage 0's "full"
+        // barrier, so the MMA wait on it runs out.  (With FUSED_DQ the packed
+        // codes still come in below: the dequant warps stay in step with the
+        // ring and never arrive twice in one phase.)
+        const bool stall = p.debug_stall && g == 0 && pair == 0 && rank == 0;
+        if (stall && !FUSED_DQ) {
           ++g;
           continue;
         }
-        uint8_t* a_dst = smem + s * kPairStageBytes;
+        uint8_t* a_dst = smem + s * kStage;
         uint8_t* b_dst = a_dst + kATileBytes;
         const uint32_t bar = full0 + s * 8u;
+        if (FUSED_DQ && it < nkb) {
+          // A by TMA; B arrives as packed codes + absmax and is expanded in smem
+          const int kel = it * 64;
+          uint8_t* r_dst = b_dst + kATileBytes;
+          if (!stall) {
+            if (rank == 0) mbar_arrive_expect_tx_ws(&full[s], tx_a_pair);
+            tma_load_2d_pair_hint_ws(a_dst, &tmA, bar, kel, m0, pol_a);
+          }
+          mbar_arrive_expect_tx_ws(&raw_full[s], tx_raw);
+          if (B_MN) {
+            // rows = reduction index n (64 of them), 128 output columns k
+            tma_load_2d_ws(r_dst, &tmB, &raw_full[s], n0 / 2, kel);
+            tma_load_2d_ws(r_dst + 4096, &tmS, &raw_full[s], (n0 / 64) & ~3, kel);
+          } else {
+            // rows = output index n (128 of them), 64 reduction columns k
+            tma_load_2d_ws(r_dst, &tmB, &raw_full[s], kel / 2, n0);
+            tma_load_2d_ws(r_dst + 4096, &tmS, &raw_full[s], it & ~3, n0);
+          }
+          raw_issued |= 1u;
+          ++g;
+          continue;
+        }
+        if (FUSED_DQ) {
+          // rank-r step: nothing to expand, but the staging barrier still
+          // completes one phase per ring round so its parity tracks `g`
+          if (lane == 0) mbar_arrive(&raw_full[s]);
+          __syncwarp();
+        }
         if (rank == 0) mbar_arrive_expect_tx_ws(&full[s], tx_pair);
         if (it < nkb) {
           const int kel = it * 64;
@@ -145,9 +231,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         ++g;
       }
     }
-    if (rank == 0 && lane == 0) {
+    if (lane == 0) {
       const uint32_t S = static_cast<uint32_t>(p.stages);
-      for (uint32_t q = (g > S ? g - S : 0u); q < g; ++q) mbar_wait(&full[q % S], (q / S) & 1u, p.timeout_ns);
+      for (uint32_t q = (g > S ? g - S : 0u); q < g; ++q) {
+        if (rank == 0) mbar_wait(&full[q % S], (q / S) & 1u, p.timeout_ns);
+        if (FUSED_DQ && ((raw_issued >> (g - 1 - q)) & 1u)) mbar_wait(&raw_full[q % S], (q / S) & 1u, p.timeout_ns);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -182,7 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + s * kPairStageBytes);
+          const uint32_t a_addr = smem_u32(smem + s * kStage);
           const uint32_t b_addr = a_addr + kATileBytes;
           if (it < nkb) {
             const uint64_t bd = B_MN ? sdesc_sw128(b_addr, 8192u, 1024u) : sdesc_sw128(b_addr, 16u, 1024u);
@@ -203,7 +292,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       }
       tc_commit_pair_multicast_ws(mma_done, 0x3);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 6) {
     // ---------------- Epilogue (both CTAs, own 128 rows) ----------------
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -248,6 +337,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
       if (lane == 0) {
         if (rank == 0) mbar_arrive(&tempty[acc]);
         else mbar_arrive_cluster(tempty0 + acc * 8u);
+      }
+    }
+  }
+  else if (FUSED_DQ && warp >= 6) {
+    // ---------------- In-kernel dequantisation (both CTAs, this CTA's half of B) ----------------
+    const int t = threadIdx.x - 6 * 32;  // 0..255
+    const uint32_t full_s0 = full0;      // even CTA's full barriers (cluster address)
+    uint32_t g = 0;
+    bool ok = true;
+    for (int tile = pair; tile < total && ok; tile += npairs) {
+      const int nt = tile / p.m_tiles;
+      const int n0 = nt * 256 + static_cast<int>(rank) * 128;
+      const int n_iter = nkb + (has_lora ? p.lora_atoms : 0);
+      for (int it = 0; it < n_iter; ++it) {
+        const uint32_t s = g % static_cast<uint32_t>(p.stages);
+        const uint32_t ph = (g / static_cast<uint32_t>(p.stages)) & 1u;
+        // one staging phase per ring round (rank-r rounds complete it with a plain arrive)
+        if (!warp_wait(&raw_full[s], ph, p.timeout_ns, abort_flag)) {
+          if (lane == 0) {
+            if (!*abort_flag) report(p, 16u);
+            *abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        if (it < nkb) {
+          uint8_t* b_blk = smem + s * kStage + kATileBytes;
+          const uint8_t* rw = b_blk + kATileBytes;
+          const float* am_box = reinterpret_cast<const float*>(rw + 4096);
+          if (B_MN) {
+            // 64 reduction rows x 128 output columns: thread -> row t/4, 32 columns
+            const int row = t >> 2, q4 = t & 3, h = q4 >> 1;
+            const float am = am_box[row * 4 + ((n0 >> 6) & 3) + h];
+            dq_row32(rw + row * 64 + q4 * 16, am, cb_s, b_blk + h * 8192, row, (q4 & 1) * 4);
+          } else {
+            // 128 output rows x 64 reduction columns: thread -> row t/2, 32 columns
+            const int row = t >> 1, hh = t & 1;
+            const float am = am_box[row * 4 + (it & 3)];
+            dq_row32(rw + row * 32 + hh * 16, am, cb_s, b_blk, row, hh * 4);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> visible to the tensor core
+        }
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0) mbar_arrive(&full[s]);
+          else mbar_arrive_cluster(full_s0 + s * 8u);
+        }
+        ++g;
       }
     }
   }

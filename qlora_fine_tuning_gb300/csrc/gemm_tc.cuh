@@ -74,6 +74,8 @@ struct GemmArgs {
   int32_t debug_stall;  // test hook: CTA (pair) 0 never fills its first stage
   int32_t l2_hints;     // bit 0: streaming (evict-first) output stores;
                         // bit 1: A loads evict-last; bit 2: B loads evict-first
+  const float* codebook;  // 16 fp32 values (pair kernel with in-kernel dequantisation)
+  int32_t dq_k;           // K of the 4-bit weight (pair kernel with in-kernel dequantisation)
 };
 
 struct TileInfo {

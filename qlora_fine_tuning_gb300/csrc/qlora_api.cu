@@ -131,6 +131,30 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map without swizzle for the packed codes (uint8) and absmax (fp32).
+bool make_map_plain(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int64_t inner, int64_t outer,
+                    int64_t ld_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Maps of the 4-bit weight for the pair kernel's in-kernel dequantisation.
+// Forward (B K-major): boxes of 128 output rows; dX (B MN-major): boxes of 64
+// reduction rows x 128 output columns.
+bool make_w4_maps(CUtensorMap* codes, CUtensorMap* scales, const qlora_w4* W, bool for_dx) {
+  const int64_t N = W->N, K = W->K;
+  const uint32_t rows = for_dx ? 64u : 128u;
+  return make_map_plain(codes, W->idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, for_dx ? 64u : 32u, rows) &&
+         make_map_plain(scales, W->absmax, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, K / 64, N, (K / 64) * 4, 4u, rows);
+}
+
 // ---------------------------------------------------------------------------
 // Shapes, workspace
 // ---------------------------------------------------------------------------
@@ -345,20 +369,30 @@ bool pair_enabled() {
   return !(e && e[0] == '1');
 }
 
-template <bool B_MN>
+// The pair kernel's in-kernel dequantisation runs on request
+// (QLORA_FUSED_DQ=1; slower than the standalone dequant on GB300) and needs
+// the absmax rows 16-byte strided (K % 256).
+bool fused_dq_ok(const qlora_w4* W) {
+  const char* e = std::getenv("QLORA_FUSED_DQ");
+  return e && e[0] == '1' && (W->K % 256 == 0);
+}
+
+template <bool B_MN, bool FUSED>
 qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles, const CUtensorMap& a,
-                              const CUtensorMap& b, const CUtensorMap& a2, const CUtensorMap& b2, GemmArgs args,
-                              cudaStream_t st) {
+                              const CUtensorMap& b, const CUtensorMap& a2, const CUtensorMap& b2,
+                              const CUtensorMap& sc, GemmArgs args, cudaStream_t st) {
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  const size_t smem = size_t(kPairStages) * kPairStageBytes + 1024 + 256;
+  const int stages = FUSED ? 5 : kPairStages;
+  const size_t smem = size_t(stages) * (FUSED ? kPairDqStageBytes : kPairStageBytes) + 1024 + 512;
   std::call_once(attr_once[dev & 63], [smem] {
-    cudaFuncSetAttribute(gemm_pair_kernel<B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaFuncSetAttribute(gemm_pair_kernel<B_MN, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
   });
   args.bn = 256;
-  args.stages = kPairStages;
-  args.stage_bytes = kPairStageBytes;
+  args.stages = stages;
+  args.stage_bytes = FUSED ? kPairDqStageBytes : kPairStageBytes;
   args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   args.debug_stall = take_stall(name) ? 1 : 0;
   args.l2_hints = l2_hints();
@@ -369,8 +403,8 @@ qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles
   cudaError_t e;
   {
     LaunchScope ls(name, st);
-    e = launch_k(gemm_pair_kernel<B_MN>, dim3(static_cast<unsigned>(2 * pairs)), dim3(192), smem, st, a, b, a2, b2,
-                 args);
+    e = launch_k(gemm_pair_kernel<B_MN, FUSED>, dim3(static_cast<unsigned>(2 * pairs)), dim3(FUSED ? 448 : 192),
+                 smem, st, a, b, a2, b2, sc, args);
   }
   return cuda_status(e);
 }
@@ -572,8 +606,13 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
   float* part = reinterpret_cast<float*>(w8 + L.off_part);
   const int64_t R = L.R;
 
-  // 1. Wd = deq(W)
-  QL_TRY(launch_dequant(W, Wd, nullptr, st));
+  // 1. Wd = deq(W), unless the pair GEMM dequantises in shared memory
+  bool b256 = true;
+  for (int j = 1; j < n_seg; ++j)
+    if (sg.start[j] % 256 != 0) b256 = false;
+  const bool pair_fwd = b256 && pair_enabled();
+  const bool fused_fwd = pair_fwd && fused_dq_ok(W);
+  if (!fused_fwd) QL_TRY(launch_dequant(W, Wd, nullptr, st));
   // 2. A^T [R,K], B^T [N,Rp] (zero columns r..Rp-1)
   {
     const TransposeJob jobs[2] = {tjob(A, K, R, R, At, R, K, K), tjob(B, r, N, N, Bt, N, L.Rp, L.Rp)};
@@ -612,16 +651,18 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
 
   // 4. Y = X . Wd^T + (s XA) . B
   {
-    bool b256 = true;
-    for (int j = 1; j < n_seg; ++j)
-      if (sg.start[j] % 256 != 0) b256 = false;
-    const bool pair = b256 && pair_enabled();
+    const bool pair = pair_fwd;
     const int bn = b256 ? 256 : 128;
     const TileCfg tc = tile_cfg(bn);
     const uint32_t brows = pair ? 128u : static_cast<uint32_t>(bn);  // rows of B staged per CTA
-    if (!make_map(&mWd, Wd, K, N, K, brows) || !make_map(&mXAs, XAs, R, M, R, 128) ||
-        !make_map(&mBt, Bt, L.Rp, N, L.Rp, brows))
-      return QLORA_ERR_CUDA;
+    CUtensorMap mSc;
+    if (fused_fwd) {
+      if (!make_w4_maps(&mWd, &mSc, W, false)) return QLORA_ERR_CUDA;
+    } else {
+      if (!make_map(&mWd, Wd, K, N, K, brows)) return QLORA_ERR_CUDA;
+      mSc = mWd;
+    }
+    if (!make_map(&mXAs, XAs, R, M, R, 128) || !make_map(&mBt, Bt, L.Rp, N, L.Rp, brows)) return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(M);
     g.N = static_cast<int32_t>(N);
@@ -635,8 +676,13 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     g.out_ld = static_cast<int32_t>(N);
     g.out_valid = static_cast<int32_t>(N);
     g.out = Y;
-    if (pair) {
-      QL_TRY(launch_gemm_pair<false>("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, g, st));
+    g.codebook = W->codebook;
+    g.dq_k = static_cast<int32_t>(K);
+    if (fused_fwd) {
+      QL_TRY((launch_gemm_pair<false, true>("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, mSc, g, st)));
+    } else if (pair) {
+      QL_TRY((launch_gemm_pair<false, false>("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, mSc, g,
+                                             st)));
     } else {
       dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(N, bn)), 1);
       QL_TRY((launch_gemm<false, false>("gemm_fwd", grid, tc, mX, mWd, mXAs, mBt, g, st)));
@@ -714,12 +760,18 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
   // 2. dX = dY . Wd + (s G) . A^T
   if (dX) {
     const bool pair = pair_enabled();
+    const bool fused = pair && fused_dq_ok(W);
     const int bn = 256;
     const TileCfg tc = tile_cfg(bn);
-    if (pair) {
+    CUtensorMap mSc;
+    if (fused) {
+      // the pair kernel expands the 4-bit codes into its MN-major B tiles
+      if (!make_w4_maps(&mWdT, &mSc, W, true)) return QLORA_ERR_CUDA;
+    } else if (pair) {
       // row-major Wd [N,K], read MN-major by the pair kernel
       QL_TRY(launch_dequant(W, WdT, nullptr, st));
       if (!make_map(&mWdT, WdT, K, N, K, 64)) return QLORA_ERR_CUDA;
+      mSc = mWdT;
     } else {
       dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(cdiv(N, 64)));
       {
@@ -744,8 +796,12 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     g.out_ld = static_cast<int32_t>(K);
     g.out_valid = static_cast<int32_t>(K);
     g.out = dX;
-    if (pair) {
-      QL_TRY(launch_gemm_pair<true>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, g, st));
+    g.codebook = W->codebook;
+    g.dq_k = static_cast<int32_t>(K);
+    if (fused) {
+      QL_TRY((launch_gemm_pair<true, true>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, mSc, g, st)));
+    } else if (pair) {
+      QL_TRY((launch_gemm_pair<true, false>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, mSc, g, st)));
     } else {
       dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(K, bn)), 1);
       QL_TRY((launch_gemm<false, false>("gemm_dx", grid, tc, mdY, mWdT, mGs, mA, g, st)));

@@ -1,0 +1,81 @@
+"""The pair GEMM with the 4-bit weight expanded inside the kernel (opt-in,
+QLORA_FUSED_DQ=1).  Its expansion is the same fp32 product and bf16
+rounding as dequant_4bit and the MMA order is unchanged, so Y and dX must be
+bit-identical to the default path; everything must also meet the oracle bound."""
+import numpy as np
+import pytest
+
+from qlora_fine_tuning_gb300 import binding, synth
+
+from harness import GpuLayer, compare, oracle_full, oracle_sampled, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.lib()
+    yield
+
+
+def _run(li, fused, monkeypatch):
+    if fused:
+        monkeypatch.setenv("QLORA_FUSED_DQ", "1")
+    else:
+        monkeypatch.delenv("QLORA_FUSED_DQ", raising=False)
+    g = GpuLayer(li)
+    g.forward()
+    g.backward()
+    g.check()
+    return g.results()
+
+
+@pytest.mark.parametrize("M,N,K,r,s,seg", [
+    (256, 1024, 1024, 8, 2.0, None),
+    (300, 512, 512, 64, 0.25, None),              # ragged M
+    (200, 1024, 512, 16, 1.0, (512, 256, 256)),   # three adapters
+    (2048, 2560, 512, 16, 1.0, None),             # several tiles per CTA pair
+])
+def test_fused_dequant_matches_default_bitwise_and_oracle(M, N, K, r, s, seg, monkeypatch):
+    li = synth.make_linear(M, N, K, r, s, seg_n=seg, seed=M + N)
+    fused = _run(li, True, monkeypatch)
+    plain = _run(li, False, monkeypatch)
+    for k in ("Y", "dX", "dA", "dB", "XA"):
+        assert np.array_equal(fused[k], plain[k]), k
+    compare(fused, oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
+
+
+@pytest.mark.slow
+def test_fused_dequant_full_size_q_proj(monkeypatch):
+    label, kw = synth.WORKLOADS["llama3-8b-q_proj-m4096-k4096-n4096-r16"][0]
+    li = synth.make_linear(seed=0, stream=0, **kw)
+    got = _run(li, True, monkeypatch)
+    idx = sample_indices(li)
+    rows, kidx, Jidx, cidx, nidx = idx
+    ref = oracle_sampled(li, idx)
+    sub = {"Y": got["Y"][rows], "dX": got["dX"][rows], "XA": got["XA"][rows],
+           "dA": got["dA"][np.ix_(kidx, Jidx)], "dB": got["dB"][np.ix_(cidx, nidx)]}
+    compare(sub, ref, keys=("Y", "dX", "dA", "dB", "XA"))
+
+
+@pytest.mark.parametrize("label", ["gemm_fwd", "gemm_dx"])
+def test_fused_dequant_stall_reports_timeout(label, monkeypatch):
+    monkeypatch.setenv("QLORA_FUSED_DQ", "1")
+    binding.qlora_set_wait_limit_ns(50_000_000)
+    try:
+        li = synth.make_linear(256, 512, 512, 16, 1.0, seed=78)
+        g = GpuLayer(li)
+        binding.qlora_debug_stall_next_launch(label)
+        g.forward()
+        g.backward()
+        assert binding.qlora_check_device_error(g.ws) == binding.TIMEOUT
+        g.forward()
+        g.backward()
+        assert binding.qlora_check_device_error(g.ws) == binding.OK
+        compare(g.results(), oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
+    finally:
+        binding.qlora_debug_stall_next_launch(None)
+        binding.qlora_set_wait_limit_ns(2_000_000_000)

@@ -107,6 +107,7 @@ SMALL = [
     (130, 384, 128, 128, 2.0, None),          # largest rank: two 64-wide LoRA blocks
     (200, 320, 128, 16, 1.0, (128, 128, 64)), # three adapters side by side
     (64, 384, 192, 8, 2.0, (256, 128)),       # rank 8 with two adapters
+    (2048, 2560, 512, 16, 1.0, None),         # more tiles than CTA pairs; rank-r rounds between tiles
 ]
 
 
