@@ -69,6 +69,31 @@ __device__ __forceinline__ void dq_row32(const uint8_t* packed16, float am, cons
   }
 }
 
+// Tile order.  group_m > 0: bands of group_m row tiles, the row tile running
+// fastest within a band, then the column tile.  group_m < 0: bands of
+// -group_m column tiles, the column tile running fastest, then the row tile.
+// Tiles processed at the same time then share one band of an operand, which
+// stays in L2 while the other operand streams past it once per band.
+__device__ __forceinline__ void pair_tile_coords(const GemmArgs& p, int tile, int& mt, int& nt) {
+  if (p.group_m < 0 && -p.group_m < p.n_tiles) {
+    const int gn = -p.group_m;
+    const int band_tiles = gn * p.m_tiles;
+    const int band = tile / band_tiles;
+    const int in_band = tile - band * band_tiles;
+    const int cols = min(gn, p.n_tiles - band * gn);  // the last band may be narrower
+    nt = band * gn + in_band % cols;
+    mt = in_band / cols;
+    return;
+  }
+  const int gm = (p.group_m > 0 && p.group_m < p.m_tiles) ? p.group_m : p.m_tiles;
+  const int band_tiles = gm * p.n_tiles;
+  const int band = tile / band_tiles;
+  const int in_band = tile - band * band_tiles;
+  const int rows = min(gm, p.m_tiles - band * gm);
+  mt = band * gm + in_band % rows;
+  nt = in_band / rows;
+}
+
 // B_MN: B is read MN-major (its rows are reduction rows holding 64 output
 // columns each; used for dX straight from the row-major dequantised weight).
 // With FUSED_DQ, tmB maps the packed codes (uint8 [N, K/2]) and tmS the
@@ -154,7 +179,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192
     uint32_t raw_issued = 0;  // bit i: ring position g-1-i had a packed-code load in flight
     bool ok = true;
     for (int tile = pair; tile < total && ok; tile += npairs) {
-      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      int mt, nt;
+      pair_tile_coords(p, tile, mt, nt);
       const int m0 = mt * 256 + static_cast<int>(rank) * 128;  // this CTA's rows of A / output
       const int nb = nt * 256;
       const int n0 = nb + static_cast<int>(rank) * 128;        // this CTA's rows of B
@@ -298,7 +324,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192
     const int row = q * 32 + lane;
     int j = 0;
     for (int tile = pair; tile < total; tile += npairs, ++j) {
-      const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+      int mt, nt;
+      pair_tile_coords(p, tile, mt, nt);
       const uint32_t acc = static_cast<uint32_t>(j & 1);
       if (!warp_wait(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
         if (lane == 0) {
@@ -347,7 +374,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192
     uint32_t g = 0;
     bool ok = true;
     for (int tile = pair; tile < total && ok; tile += npairs) {
-      const int nt = tile / p.m_tiles;
+      int mt, nt;
+      pair_tile_coords(p, tile, mt, nt);
       const int n0 = nt * 256 + static_cast<int>(rank) * 128;
       const int n_iter = nkb + (has_lora ? p.lora_atoms : 0);
       for (int it = 0; it < n_iter; ++it) {

@@ -4,17 +4,20 @@
 //   (+ optional rank-r "LoRA" K-steps A2[row, :] * B2[col, :] into the same
 //    TMEM accumulator).
 //
-// Every contraction of the QLoRA linear layer is an instance:
-//   XA  = X . A            (A-op X K-major, B-op A^T)          fp32 split-K partials
+// The rank-r contractions of the QLoRA linear layer are instances whose
+// reduction splits are summed inside the kernel (EPI_RED, below):
+//   XA  = X . A            (A-op X K-major, B-op A read MN-major)   -> XA, s*XA
+//   G   = dY . B^T per adapter segment (B-op B K-major)           -> s*G, G
+//   dA  = s X^T G          (A-op X read MN-major, B-op G MN-major)  -> dA fp32
+//   dB^T= s dY^T . XA      (A-op dY read MN-major, B-op XA MN-major) -> dB fp32
+// and, when the CTA-pair kernel cannot be used, the two large products
 //   Y   = X . Wd^T + (s XA) . B    (B-op Wd; LoRA: A2 = s*XA, B2 = B^T)  bf16
-//   G   = dY . B^T per adapter segment                         fp32 split partials
 //   dX  = dY . Wd + (s G) . A^T    (B-op Wd^T; LoRA: A2 = s*G, B2 = A)  bf16
-//   dA  = X^T . G          (A-op X read MN-major, B-op G^T)    fp32 split partials
-//   dB^T= dY^T . XA        (A-op dY read MN-major, B-op XA^T)  fp32 split partials
 //
-// Persistent: each CTA walks the tile list (row tile fastest, then column
-// tile, then split/segment) with stride gridDim.x.  Roles (6 warps):
-//   warp 0 lane 0  TMA producer, runs ahead across tile boundaries through a
+// Persistent: each CTA (or cluster, EPI_RED) walks the tile list (row tile
+// fastest, then column tile, then segment) with a fixed stride.  Roles
+// (6 warps):
+//   warp 0         TMA producer, runs ahead across tile boundaries through a
 //                  ring of `stages` shared-memory stages;
 //   warp 1         MMA issuer: tcgen05.mma (M=128, N=bn, K=16) into one of two
 //                  TMEM accumulators (tile j uses buffer j&1);
@@ -23,11 +26,20 @@
 //                  overlaps the mainloop of tile j+1.
 // Warp 0 owns the TMEM allocation (2 x bn columns rounded to a power of two).
 //
+// EPI_RED: the `splits` CTAs that share one output tile form a thread-block
+// cluster; CTA k reduces over the k-th chunk of the reduction.  Each CTA
+// copies its fp32 accumulator to a shared-memory buffer, then sums one slice
+// of the tile's rows over all buffers of the cluster (distributed shared
+// memory), in split order 0, 1, ..., so the result does not depend on timing,
+// and writes the outputs.  Two mbarriers per CTA pace the exchange: red_ready
+// (every CTA's buffer of this round is written) and red_free (every CTA has
+// read this CTA's buffer).  No partial sums go through global memory.
+//
 // Shared-memory tiles use the 128-byte swizzle written by TMA:
 //   K-major operand  : row i at i*128 B holds 64 reduction elements; 8-row
 //                      atoms of 1024 B (SBO = 1024); a 16-wide K step is +32 B.
 //   MN-major operand : row j at j*128 B holds 64 output-index elements for
-//                      reduction index j; 8-row atoms (SBO = 1024); the second
+//                      reduction index j; 8-row atoms (SBO = 1024); the next
 //                      64-wide output block sits 8192 B further (LBO);
 //                      a 16-wide K step is +2048 B.
 #pragma once
@@ -46,7 +58,15 @@ enum GemmMode : int32_t {
   GM_DB = 4,     // segment chosen by the output-row tile; B rows offset by seg*r
 };
 
+enum GemmEpi : int {
+  EPI_BF16 = 0,      // bf16 output tile
+  EPI_F32_PART = 1,  // fp32 partial sum per split (summed by a separate kernel)
+  EPI_RED = 2,       // splits summed in the kernel across a cluster
+};
+
 constexpr int kMaxSeg = 8;
+constexpr uint32_t kRedLd = 68;                     // floats per row of the reduction buffer (64 + 4 pad)
+constexpr uint32_t kRedBytes = 128u * kRedLd * 4u;  // one 128 x 64 fp32 chunk
 constexpr int kMaxStages = 8;
 constexpr uint32_t kATileBytes = 128 * 128;  // 128 rows x 64 bf16
 
@@ -74,8 +94,16 @@ struct GemmArgs {
   int32_t debug_stall;  // test hook: CTA (pair) 0 never fills its first stage
   int32_t l2_hints;     // bit 0: streaming (evict-first) output stores;
                         // bit 1: A loads evict-last; bit 2: B loads evict-first
+  int32_t group_m;        // pair kernel tile order: >0 row tiles per band, <0 column tiles per band, 0 one band
   const float* codebook;  // 16 fp32 values (pair kernel with in-kernel dequantisation)
   int32_t dq_k;           // K of the 4-bit weight (pair kernel with in-kernel dequantisation)
+  // EPI_RED outputs; `sum` is the full reduction, columns are shifted by out_col0:
+  float red_scale;
+  __nv_bfloat16* red_bf16;    // sum, row-major [row * red_ld + col]
+  __nv_bfloat16* red_bf16_s;  // red_scale * sum, row-major
+  float* red_f32;             // red_scale * sum, row-major
+  float* red_f32_t;           // red_scale * sum, transposed [col * red_ld_t + row]
+  int64_t red_ld, red_ld_t;
 };
 
 struct TileInfo {
@@ -144,26 +172,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <bool A_MN, bool OUT_F32>
+// Flat tile index of the T-th tile of a cluster walk (EPI_RED): the cluster
+// rank picks the split, z = segment * splits + split.
+__device__ __forceinline__ int red_tile(const GemmArgs& p, int T, uint32_t rank) {
+  const int mn = p.m_tiles * p.n_tiles;
+  return T % mn + mn * ((T / mn) * p.splits + static_cast<int>(rank));
+}
+
+template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                    const GemmArgs p) {
+  constexpr bool RED = (EPI == EPI_RED);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((((raw + 1023u) & ~1023u)) - raw);
-  uint8_t* ctrl = smem + static_cast<uint32_t>(p.stages) * p.stage_bytes;
+  float* red = reinterpret_cast<float*>(smem + static_cast<uint32_t>(p.stages) * p.stage_bytes);
+  uint8_t* ctrl = reinterpret_cast<uint8_t*>(red) + (RED ? kRedBytes : 0u);
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;   // [2] accumulator ready
   uint64_t* tempty = tfull + 2;           // [2] accumulator drained
   uint64_t* mma_done = tempty + 2;        // every MMA of this CTA completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* red_ready = mma_done + 1;     // EPI_RED: all buffers of the round written
+  uint64_t* red_free = red_ready + 1;     // EPI_RED: this CTA's buffer read by all
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_free + 1);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int total = p.m_tiles * p.n_tiles * p.z_tiles;
+  const int S = RED ? p.splits : 1;
+  const uint32_t rank = RED ? cluster_ctarank() : 0u;
+  // Tile walk: CTAs (or clusters) take every stride-th tile.
+  const int walk_first = RED ? static_cast<int>(blockIdx.x) / S : static_cast<int>(blockIdx.x);
+  const int walk_stride = RED ? static_cast<int>(gridDim.x) / S : static_cast<int>(gridDim.x);
+  const int walk_total = RED ? total / S : total;
   const bool has_lora = (p.mode == GM_FWD || p.mode == GM_DX) && p.lora_atoms > 0;
   uint32_t acc_cols = 32;
   while (acc_cols < static_cast<uint32_t>(p.bn)) acc_cols <<= 1;
@@ -179,6 +224,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&tempty[i], 4);
     }
     mbar_init(mma_done, 1);
+    if (RED) {
+      mbar_init(red_ready, static_cast<uint32_t>(S) * 128u);
+      mbar_init(red_free, static_cast<uint32_t>(S) * 128u);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -196,6 +245,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (RED) cluster_sync_all();  // peers' barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Everything above touched only on-chip state; global memory written by the
@@ -208,8 +258,8 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tx = kATileBytes + static_cast<uint32_t>(p.bn) * 128u;
     uint32_t g = 0;  // iterations issued so far (ring position)
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const TileInfo t = tile_info(p, tile);
+    for (int T = walk_first; T < walk_total && ok; T += walk_stride) {
+      const TileInfo t = tile_info(p, RED ? red_tile(p, T, rank) : T);
       for (int it = 0; it < t.n_iter; ++it) {
         const uint32_t s = g % static_cast<uint32_t>(p.stages);
         const uint32_t ph = (g / static_cast<uint32_t>(p.stages)) & 1u;
@@ -236,7 +286,12 @@ __global__ void __launch_bounds__(192, 1)
           } else {
             tma_load_2d_ws(a_dst, &tmA, &full[s], kel, t.m0);
           }
-          tma_load_2d_ws(b_dst, &tmB, &full[s], kel, t.b_row0);
+          if (B_MN) {
+            for (int i = 0; i < p.bn / 64; ++i)
+              tma_load_2d_ws(b_dst + i * 8192, &tmB, &full[s], t.b_row0 + 64 * i, kel);
+          } else {
+            tma_load_2d_ws(b_dst, &tmB, &full[s], kel, t.b_row0);
+          }
         } else {
           const int a = it - t.n_main;
           tma_load_2d_ws(a_dst, &tmA2, &full[s], t.a2_x0 + 64 * a, t.m0);
@@ -247,20 +302,21 @@ __global__ void __launch_bounds__(192, 1)
     }
     // Do not leave the CTA while copies it issued may still land in smem.
     if (lane == 0) {
-      const uint32_t S = static_cast<uint32_t>(p.stages);
-      for (uint32_t q = (g > S ? g - S : 0u); q < g; ++q) mbar_wait(&full[q % S], (q / S) & 1u, p.timeout_ns);
+      const uint32_t S_ = static_cast<uint32_t>(p.stages);
+      for (uint32_t q = (g > S_ ? g - S_ : 0u); q < g; ++q) mbar_wait(&full[q % S_], (q / S_) & 1u, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
-    const uint32_t idesc_main = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), A_MN, false);
+    const uint32_t idesc_main = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), A_MN, B_MN);
     const uint32_t idesc_lora = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), false, false);
     const uint64_t a_step = A_MN ? (2048u >> 4) : (32u >> 4);
+    const uint64_t b_step = B_MN ? (2048u >> 4) : (32u >> 4);
     uint32_t g = 0;
     int j = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++j) {
-      const TileInfo t = tile_info(p, tile);
+    for (int T = walk_first; T < walk_total && ok; T += walk_stride, ++j) {
+      const TileInfo t = tile_info(p, RED ? red_tile(p, T, rank) : T);
       const uint32_t acc = static_cast<uint32_t>(j & 1);
       if (!warp_wait(&tempty[acc], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
         if (lane == 0) {
@@ -287,8 +343,8 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t b_addr = a_addr + kATileBytes;
         if (it < t.n_main) {
           const uint64_t ad = A_MN ? sdesc_sw128(a_addr, 8192u, 1024u) : sdesc_sw128(a_addr, 16u, 1024u);
-          tc_mma_bf16_k64_ws(d_tmem, ad, sdesc_sw128(b_addr, 16u, 1024u), a_step, 2u, idesc_main,
-                             it > 0 ? 1u : 0u);
+          const uint64_t bd = B_MN ? sdesc_sw128(b_addr, 8192u, 1024u) : sdesc_sw128(b_addr, 16u, 1024u);
+          tc_mma_bf16_k64_ws(d_tmem, ad, bd, a_step, b_step, idesc_main, it > 0 ? 1u : 0u);
         } else {
           const int ksteps = min(4, p.lora_ksteps - 4 * (it - t.n_main));
           for (int kk = 0; kk < ksteps; ++kk)
@@ -303,13 +359,198 @@ __global__ void __launch_bounds__(192, 1)
       tc_commit_ws(&tfull[acc]);  // arrives once this tile's MMAs have completed
     }
     tc_commit_ws(mma_done);
+  } else if (warp >= 2 && RED) {
+    // ---------------- Epilogue: sum the splits across the cluster ----------------
+    if constexpr (RED) {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    const int et = static_cast<int>(threadIdx.x) - 64;  // 0..127
+    const int rs = (128 + S - 1) / S;                    // rows this CTA sums
+    const int lo = min(128, static_cast<int>(rank) * rs);
+    const int nrows = min(128, lo + rs) - lo;
+    const uint32_t red_s = smem_u32(red);
+    const uint32_t ready_s = smem_u32(red_ready);
+    const uint32_t free_s = smem_u32(red_free);
+    uint32_t round = 0;
+    int j = 0;
+    bool ok = true;
+    for (int T = walk_first; T < walk_total && ok; T += walk_stride, ++j) {
+      const TileInfo t = tile_info(p, red_tile(p, T, rank));
+      const uint32_t acc = static_cast<uint32_t>(j & 1);
+      if (!warp_wait(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
+        if (lane == 0) {
+          if (!*abort_flag) report(p, 4u);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t_base = tmem_base + acc * acc_cols + (static_cast<uint32_t>(q * 32) << 16);
+      if (S == 1) {
+        // One split: the accumulator is the sum; store straight from registers.
+        const int grow = t.m0 + row;
+        for (int c = 0; c < p.bn; c += 16) {
+          uint32_t v[16];
+          if (t.n_iter > 0) {
+            tmem_ld16(t_base + static_cast<uint32_t>(c), v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0u;
+          }
+          if (grow >= p.M) continue;
+          const int gcol = t.n0 + c;
+          const int lim = min(p.out_valid, p.N);
+          if (p.red_f32_t) {
+            // a warp's 32 rows are 32 consecutive outputs of each column
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (gcol + e < lim)
+                p.red_f32_t[static_cast<int64_t>(gcol + e + t.out_col0) * p.red_ld_t + grow] =
+                    __fmul_rn(p.red_scale, __uint_as_float(v[e]));
+          } else {
+            const int64_t o = static_cast<int64_t>(grow) * p.red_ld + t.out_col0 + gcol;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (gcol + 8 * h >= lim) continue;
+              const float* f = reinterpret_cast<const float*>(v) + 8 * h;
+              if (p.red_bf16)
+                *reinterpret_cast<uint4*>(p.red_bf16 + o + 8 * h) =
+                    make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                               pack_bf16x2(f[6], f[7]));
+              if (p.red_bf16_s) {
+                float g8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) g8[e] = __fmul_rn(p.red_scale, f[e]);
+                *reinterpret_cast<uint4*>(p.red_bf16_s + o + 8 * h) =
+                    make_uint4(pack_bf16x2(g8[0], g8[1]), pack_bf16x2(g8[2], g8[3]), pack_bf16x2(g8[4], g8[5]),
+                               pack_bf16x2(g8[6], g8[7]));
+              }
+              if (p.red_f32) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e)
+                  *reinterpret_cast<float4*>(p.red_f32 + o + 8 * h + 4 * e) =
+                      make_float4(__fmul_rn(p.red_scale, f[4 * e]), __fmul_rn(p.red_scale, f[4 * e + 1]),
+                                  __fmul_rn(p.red_scale, f[4 * e + 2]), __fmul_rn(p.red_scale, f[4 * e + 3]));
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        continue;
+      }
+      for (int c64 = 0; c64 < p.bn; c64 += 64, ++round) {
+        const int cw = min(64, p.bn - c64);
+        // 1. this CTA's buffer has been read by every CTA in the previous round
+        if (!warp_wait_cluster(red_free, (round & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        // 2. accumulator columns [c64, c64 + cw) -> buffer row `row`
+        for (int c = 0; c < cw; c += 16) {
+          uint32_t v[16];
+          if (t.n_iter > 0) {
+            tmem_ld16(t_base + static_cast<uint32_t>(c64 + c), v);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = 0u;
+          }
+          float4* dst = reinterpret_cast<float4*>(red + row * kRedLd + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                 __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+        }
+        if (c64 + 64 >= p.bn) {  // accumulator read out: the MMA warp may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[acc]);
+        }
+        // 3. publish: arrive (release) on every CTA's red_ready
+        for (int k = 0; k < S; ++k) mbar_arrive_cluster(mapa_shared(ready_s, static_cast<uint32_t>(k)));
+        // 4. every buffer of this round is written
+        if (!warp_wait_cluster(red_ready, round & 1u, p.timeout_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        // 5. sum rows [lo, lo + nrows) over the cluster in split order; a
+        //    thread takes groups of 4 columns, kB groups at a time so that
+        //    kB loads are in flight per split.  Row-major outputs walk the
+        //    groups row by row, the transposed output column-group by
+        //    column-group (consecutive threads -> consecutive rows).
+        constexpr int kB = 4;
+        const int g4 = cw / 4;
+        const int items = nrows * g4;
+        const bool tr = p.red_f32_t != nullptr;
+        for (int base = et; base < items; base += 128 * kB) {
+          uint32_t off[kB];
+          int rr[kB], cc[kB];
+          float4 sum[kB];
+#pragma unroll
+          for (int i = 0; i < kB; ++i) {
+            const int e = min(base + 128 * i, items - 1);
+            rr[i] = lo + (tr ? e % nrows : e / g4);
+            cc[i] = 4 * (tr ? e / nrows : e % g4);
+            off[i] = red_s + static_cast<uint32_t>(rr[i] * kRedLd + cc[i]) * 4u;
+            sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          for (int k = 0; k < S; ++k) {
+            float4 v[kB];
+#pragma unroll
+            for (int i = 0; i < kB; ++i) v[i] = ld_shared_cluster_v4(mapa_shared(off[i], static_cast<uint32_t>(k)));
+#pragma unroll
+            for (int i = 0; i < kB; ++i) {
+              sum[i].x += v[i].x;
+              sum[i].y += v[i].y;
+              sum[i].z += v[i].z;
+              sum[i].w += v[i].w;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kB; ++i) {
+            if (base + 128 * i >= items) break;
+            const int grow = t.m0 + rr[i], gcol = t.n0 + c64 + cc[i];
+            if (grow >= p.M || gcol >= p.out_valid || gcol >= p.N) continue;
+            const float f[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
+            if (tr) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                p.red_f32_t[static_cast<int64_t>(gcol + e + t.out_col0) * p.red_ld_t + grow] =
+                    __fmul_rn(p.red_scale, f[e]);
+              continue;
+            }
+            const int64_t o = static_cast<int64_t>(grow) * p.red_ld + t.out_col0 + gcol;
+            if (p.red_bf16)
+              *reinterpret_cast<uint2*>(p.red_bf16 + o) = make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+            if (p.red_bf16_s)
+              *reinterpret_cast<uint2*>(p.red_bf16_s + o) =
+                  make_uint2(pack_bf16x2(__fmul_rn(p.red_scale, f[0]), __fmul_rn(p.red_scale, f[1])),
+                             pack_bf16x2(__fmul_rn(p.red_scale, f[2]), __fmul_rn(p.red_scale, f[3])));
+            if (p.red_f32)
+              *reinterpret_cast<float4*>(p.red_f32 + o) =
+                  make_float4(__fmul_rn(p.red_scale, f[0]), __fmul_rn(p.red_scale, f[1]),
+                              __fmul_rn(p.red_scale, f[2]), __fmul_rn(p.red_scale, f[3]));
+          }
+        }
+        // 6. done reading this round: arrive (release) on every CTA's red_free
+        for (int k = 0; k < S; ++k) mbar_arrive_cluster(mapa_shared(free_s, static_cast<uint32_t>(k)));
+      }
+    }
+    if (!ok && lane == 0) {
+      if (!*abort_flag) report(p, 32u);
+      *abort_flag = 1;
+    }
+    }  // if constexpr (RED)
   } else if (warp >= 2) {
     // ---------------- Epilogue ----------------
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     int j = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++j) {
-      const TileInfo t = tile_info(p, tile);
+    for (int T = walk_first; T < walk_total; T += walk_stride, ++j) {
+      const TileInfo t = tile_info(p, T);
       const uint32_t acc = static_cast<uint32_t>(j & 1);
       if (!warp_wait(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
         if (lane == 0) {
@@ -335,7 +576,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         const int c0 = t.n0 + c * 16;
         if (!row_ok) continue;
-        if (OUT_F32) {
+        if (EPI == EPI_F32_PART) {
           float* out = reinterpret_cast<float*>(p.out) + static_cast<int64_t>(t.split) * p.out_split_stride +
                        static_cast<int64_t>(grow) * p.out_ld + t.out_col0;
 #pragma unroll
@@ -377,6 +618,9 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, tmem_cols);
   }
+  // No CTA leaves while a peer may still read its buffer or arrive on its
+  // barriers (every wait above is bounded, so all threads get here).
+  if (RED) cluster_sync_all();
 }
 
 }  // namespace qlora

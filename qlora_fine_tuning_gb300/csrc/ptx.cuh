@@ -183,6 +183,36 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// 16-byte load from shared memory of a CTA of this cluster (cluster address).
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+// Phase test with acquire at cluster scope: writes that other CTAs of the
+// cluster released before arriving are visible after it succeeds.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -385,6 +415,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
                                           volatile int32_t* abort_flag) {
   if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   return warp_wait_slow(bar, parity, limit_ns, abort_flag);
+}
+
+// Whole-warp bounded wait where every lane acquires at cluster scope (each
+// lane then reads what other CTAs of the cluster wrote).
+__device__ __noinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                               volatile int32_t* abort_flag) {
+  const uint64_t t0 = globaltimer_ns();
+  bool done = false;
+  while (true) {
+    if (!done) done = mbar_try_wait_cluster(bar, parity);
+    if (__all_sync(0xffffffffu, done)) return true;
+    const bool stop = (*abort_flag != 0) || (globaltimer_ns() - t0 > limit_ns);
+    if (__any_sync(0xffffffffu, stop)) return false;
+  }
 }
 
 }  // namespace qlora

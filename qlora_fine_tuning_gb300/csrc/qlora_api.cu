@@ -163,6 +163,12 @@ inline int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 constexpr int kSMs = 152;
 
 // Number of SMs of device `dev` (cached; 152 on GB300).
+int cur_dev() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
 int sm_count(int dev) {
   static std::atomic<int> cache[64];
   int v = cache[dev & 63].load(std::memory_order_relaxed);
@@ -175,23 +181,12 @@ constexpr int kMaxSplits = 8;
 
 // Split count that depends only on the reduction length, so that a row's
 // result never depends on how many rows are in the batch.
-int splits_for_rows(int64_t nkb) {
-  return static_cast<int>(std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, cdiv(nkb, 32))));
-}
-
-int choose_splits(int64_t tiles, int64_t nkb) {
-  int64_t s = std::max<int64_t>(1, kSMs / std::max<int64_t>(1, tiles));  // never more tiles than one wave
-  s = std::min<int64_t>(s, kMaxSplits);
-  s = std::min<int64_t>(s, std::max<int64_t>(1, nkb));
-  return static_cast<int>(s);
-}
-
 // Workspace header: the device error word (first 4 bytes of 256).
 constexpr size_t kHeaderBytes = 256;
 
 struct Layout {
   int64_t M, N, K, r, nseg, R, Rp, Mp;
-  size_t off_err, off_wd, off_bt, off_at, off_xas, off_xat, off_gt, off_part, total;
+  size_t off_err, off_wd, off_bt, off_xas, off_g, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -206,24 +201,18 @@ Layout layout(int64_t M, int64_t N, int64_t K, int64_t r, int64_t nseg) {
   L.R = r * nseg;
   L.Rp = rup(r, 16);
   L.Mp = rup(std::max<int64_t>(M, 1), 8);
+  const size_t rows = size_t(std::max<int64_t>(M, 1));
   size_t o = 0;
   L.off_err = o;
   o += kHeaderBytes;
-  L.off_wd = o;
+  L.off_wd = o;  // deq(W) [N,K] bf16
   o = align256(o + size_t(N) * K * 2);
-  L.off_bt = o;
+  L.off_bt = o;  // B^T [N,Rp] bf16, zero columns r..Rp-1 (forward)
   o = align256(o + size_t(N) * L.Rp * 2);
-  L.off_at = o;
-  o = align256(o + size_t(L.R) * K * 2);
-  L.off_xas = o;  // s*XA (forward) or s*G (backward), [M,R]
-  o = align256(o + size_t(std::max<int64_t>(M, 1)) * L.R * 2);
-  L.off_xat = o;  // XA^T [R, Mp]
-  o = align256(o + size_t(L.R) * L.Mp * 2);
-  L.off_gt = o;  // G^T [R, Mp]
-  o = align256(o + size_t(L.R) * L.Mp * 2);
-  L.off_part = o;
-  const int64_t pe = std::max({std::max<int64_t>(M, 1) * L.R, K * L.R, N * L.Rp});
-  o = align256(o + size_t(kMaxSplits) * pe * 4);
+  L.off_xas = o;  // s*XA (forward) or s*G (backward), [M,R] bf16
+  o = align256(o + rows * L.R * 2);
+  L.off_g = o;  // G [M,R] bf16 (backward)
+  o = align256(o + rows * L.R * 2);
   L.total = o;
   return L;
 }
@@ -287,6 +276,33 @@ int l2_hints() {
   return v;
 }
 
+// Band of the pair GEMM's tile order (GemmArgs::group_m).  Both operands
+// have 256 rows per tile, so a tile of either is 256*K*2 bytes.  A band holds
+// as many tiles of one operand as fit in `budget` bytes of L2; the other
+// operand is then read once per band.  Modelled DRAM reads, in tiles:
+//   row bands:    ceil(m_tiles/g)*n_tiles + m_tiles
+//   column bands: ceil(n_tiles/g)*m_tiles + n_tiles
+// and the smaller wins.  QLORA_GROUP_M forces a band (signed as group_m),
+// QLORA_BAND_MB sets the budget.
+int pair_group(int64_t m_tiles, int64_t n_tiles, int64_t K) {
+  static const int forced = [] {
+    const char* e = std::getenv("QLORA_GROUP_M");
+    return e ? std::atoi(e) : 0;
+  }();
+  static const int64_t budget = [] {
+    const char* e = std::getenv("QLORA_BAND_MB");
+    const int64_t mb = e ? std::atoll(e) : 32;
+    return (mb > 0 ? mb : 32) << 20;
+  }();
+  if (forced != 0) return forced;
+  const int64_t tile_bytes = 256 * K * 2;
+  const int64_t g = std::max<int64_t>(1, budget / std::max<int64_t>(tile_bytes, 1));
+  const int64_t rows = cdiv(m_tiles, g) * n_tiles + m_tiles;
+  const int64_t cols = cdiv(n_tiles, g) * m_tiles + n_tiles;
+  const int64_t gi = std::min<int64_t>(g, 1 << 20);
+  return rows <= cols ? static_cast<int>(gi) : -static_cast<int>(gi);
+}
+
 constexpr int kSmemLimit = 232448;
 
 // Launches may overlap the tail of their predecessor in the stream
@@ -323,30 +339,32 @@ struct TileCfg {
   size_t smem;
 };
 
-TileCfg tile_cfg(int bn) {
+// Ring geometry of gemm_tc_kernel; `red` reserves the split-sum buffer.
+TileCfg tile_cfg(int bn, bool red = false) {
   TileCfg c;
   c.bn = bn;
   c.stage_bytes = static_cast<uint32_t>(rup(kATileBytes + int64_t(bn) * 128, 1024));
-  c.stages = std::min<int>(kMaxStages, static_cast<int>((200 * 1024) / c.stage_bytes));
-  c.smem = size_t(c.stages) * c.stage_bytes + 1024 + 256;
+  const int64_t ring = red ? int64_t(kSmemLimit) - kRedBytes - 1024 - 256 : 200 * 1024;
+  c.stages = std::min<int>(kMaxStages, static_cast<int>(ring / c.stage_bytes));
+  c.smem = size_t(c.stages) * c.stage_bytes + (red ? kRedBytes : 0) + 1024 + 256;
   return c;
 }
 
-template <bool A_MN, bool F32>
+template <bool A_MN, bool B_MN, int EPI>
 qlora_status launch_gemm(const char* name, dim3 grid, const TileCfg& tc, const CUtensorMap& a, const CUtensorMap& b,
                          const CUtensorMap& a2, const CUtensorMap& b2, GemmArgs args, cudaStream_t st) {
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
   std::call_once(attr_once[dev & 63], [] {
-    cudaFuncSetAttribute(gemm_tc_kernel<A_MN, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaFuncSetAttribute(gemm_tc_kernel<A_MN, B_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   });
   args.bn = tc.bn;
   args.stages = tc.stages;
   args.stage_bytes = tc.stage_bytes;
   args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   args.debug_stall = take_stall(name) ? 1 : 0;
-  args.l2_hints = F32 ? 0 : (l2_hints() & 1);
+  args.l2_hints = (EPI == EPI_BF16) ? (l2_hints() & 1) : 0;
   // `grid` is the tile grid; the kernel is persistent with one CTA per SM.
   args.m_tiles = static_cast<int32_t>(grid.x);
   args.n_tiles = static_cast<int32_t>(grid.y);
@@ -356,9 +374,109 @@ qlora_status launch_gemm(const char* name, dim3 grid, const TileCfg& tc, const C
   cudaError_t e;
   {
     LaunchScope ls(name, st);
-    e = launch_k(gemm_tc_kernel<A_MN, F32>, dim3(ctas), dim3(192), tc.smem, st, a, b, a2, b2, args);
+    e = launch_k(gemm_tc_kernel<A_MN, B_MN, EPI>, dim3(ctas), dim3(192), tc.smem, st, a, b, a2, b2, args);
   }
   return cuda_status(e);
+}
+
+// Clusters of `splits` CTAs of gemm_tc_kernel<.., EPI_RED> that fit on the
+// device at once (cached per instance, device and cluster size).
+template <bool A_MN, bool B_MN>
+int max_red_clusters(int splits, size_t smem) {
+  static std::mutex mu;
+  static int cache[64][kMaxSplits + 1] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  int& c = cache[dev & 63][splits];
+  if (c == 0) {
+    auto kern = gemm_tc_kernel<A_MN, B_MN, EPI_RED>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(splits) * 64u);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sm_count(dev) / splits;
+    }
+    c = std::max(1, n);
+  }
+  return c;
+}
+
+// Splits (cluster size) for an EPI_RED GEMM with `tiles` output tiles of
+// `nkb` 64-wide reduction blocks: the most splits, up to 8, for which all
+// clusters of one wave fit on the device at once.
+template <bool A_MN, bool B_MN>
+int red_splits(int64_t tiles, int64_t nkb, size_t smem) {
+  const int64_t cap = std::min<int64_t>({int64_t(kMaxSplits), std::max<int64_t>(1, nkb),
+                                         std::max<int64_t>(1, int64_t(sm_count(cur_dev())) / std::max<int64_t>(tiles, 1))});
+  for (int64_t sp = cap; sp > 1; --sp)
+    if (max_red_clusters<A_MN, B_MN>(static_cast<int>(sp), smem) >= tiles) return static_cast<int>(sp);
+  return 1;
+}
+
+// gemm_tc_kernel<.., EPI_RED>: tiles m_tiles x n_tiles x zseg (zseg adapter
+// segments for GM_G, else 1), `splits` CTAs per tile in one cluster.
+template <bool A_MN, bool B_MN>
+qlora_status launch_gemm_red(const char* name, int64_t m_tiles, int64_t n_tiles, int64_t zseg, int splits,
+                             const TileCfg& tc, const CUtensorMap& a, const CUtensorMap& b, GemmArgs args,
+                             cudaStream_t st) {
+  auto kern = gemm_tc_kernel<A_MN, B_MN, EPI_RED>;
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::call_once(attr_once[dev & 63], [kern] {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  });
+  args.bn = tc.bn;
+  args.stages = tc.stages;
+  args.stage_bytes = tc.stage_bytes;
+  args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  args.debug_stall = take_stall(name) ? 1 : 0;
+  args.l2_hints = 0;
+  args.splits = splits;
+  args.m_tiles = static_cast<int32_t>(m_tiles);
+  args.n_tiles = static_cast<int32_t>(n_tiles);
+  args.z_tiles = static_cast<int32_t>(zseg * splits);
+  const int64_t tiles = m_tiles * n_tiles * zseg;
+  const int64_t clusters = std::min<int64_t>(tiles, max_red_clusters<A_MN, B_MN>(splits, tc.smem));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * splits));
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = tc.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e;
+  {
+    LaunchScope ls(name, st);
+    e = cudaLaunchKernelEx(&cfg, kern, a, b, a, b, args);
+  }
+  return cuda_status(e);
+}
+
+// Splits of XA = X.A: shared by the forward and the static-scratch entry
+// point so both sum the same reduction chunks in the same order.
+int xa_splits(int64_t M, int64_t K, int64_t R) {
+  const TileCfg tc = tile_cfg(static_cast<int>(rup(R, 64)), true);
+  return red_splits<false, true>(cdiv(M, 128), K / 64, tc.smem);
 }
 
 // CTA-pair kernel for the two large GEMMs (256 x 256 tiles, K-major operands).
@@ -396,6 +514,7 @@ qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles
   args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   args.debug_stall = take_stall(name) ? 1 : 0;
   args.l2_hints = l2_hints();
+  args.group_m = pair_group(m_tiles, n_tiles, args.red_len);
   args.m_tiles = static_cast<int32_t>(m_tiles);
   args.n_tiles = static_cast<int32_t>(n_tiles);
   args.z_tiles = 1;
@@ -601,9 +720,7 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
   uint32_t* err = reinterpret_cast<uint32_t*>(w8 + L.off_err);
   void* Wd = w8 + L.off_wd;
   void* Bt = w8 + L.off_bt;
-  void* At = w8 + L.off_at;
   void* XAs = w8 + L.off_xas;
-  float* part = reinterpret_cast<float*>(w8 + L.off_part);
   const int64_t R = L.R;
 
   // 1. Wd = deq(W), unless the pair GEMM dequantises in shared memory
@@ -613,40 +730,31 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
   const bool pair_fwd = b256 && pair_enabled();
   const bool fused_fwd = pair_fwd && fused_dq_ok(W);
   if (!fused_fwd) QL_TRY(launch_dequant(W, Wd, nullptr, st));
-  // 2. A^T [R,K], B^T [N,Rp] (zero columns r..Rp-1)
+  // 2. B^T [N,Rp] (zero columns r..Rp-1): the LoRA B-operand of the Y GEMM
   {
-    const TransposeJob jobs[2] = {tjob(A, K, R, R, At, R, K, K), tjob(B, r, N, N, Bt, N, L.Rp, L.Rp)};
-    QL_TRY(launch_transposes("transpose_AB", jobs, 2, st));
+    const TransposeJob jobs[1] = {tjob(B, r, N, N, Bt, N, L.Rp, L.Rp)};
+    QL_TRY(launch_transposes("transpose_B", jobs, 1, st));
   }
 
-  // 3. XA = X . A  (split over K)
-  CUtensorMap mX, mAt, mWd, mXAs, mBt;
+  // 3. XA = X . A (A read MN-major; splits of K summed in the kernel);
+  //    writes XA_save = bf16(XA) and s*XA
+  CUtensorMap mX, mWd, mXAs, mBt;
   {
-    const int bn = static_cast<int>(rup(R, 16));
-    const TileCfg tc = tile_cfg(bn);
-    const int64_t mt = cdiv(M, 128);
-    const int splits = splits_for_rows(K / 64);
-    if (!make_map(&mX, X, K, M, K, 128) || !make_map(&mAt, At, K, R, K, static_cast<uint32_t>(bn)))
-      return QLORA_ERR_CUDA;
+    CUtensorMap mA;
+    const TileCfg tc = tile_cfg(static_cast<int>(rup(R, 64)), true);
+    const int splits = xa_splits(M, K, R);
+    if (!make_map(&mX, X, K, M, K, 128) || !make_map(&mA, A, R, K, R, 64)) return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(M);
     g.N = static_cast<int32_t>(R);
     g.mode = GM_PLAIN;
     g.red_len = static_cast<int32_t>(K);
-    g.splits = splits;
-    g.out_ld = static_cast<int32_t>(R);
     g.out_valid = static_cast<int32_t>(R);
-    g.out_split_stride = M * R;
-    g.out = part;
-    QL_TRY((launch_gemm<false, true>("gemm_xa", dim3(static_cast<unsigned>(mt), 1, splits), tc, mX, mAt, mX, mAt, g,
-                                     st)));
-    {
-      ReduceArgs ra = reduce_args(part, splits, M, R, R, M * R, s);
-      ra.out_bf16 = reinterpret_cast<__nv_bfloat16*>(XA_save);
-      ra.out_bf16_s = reinterpret_cast<__nv_bfloat16*>(XAs);
-      ra.ld_o = R;
-      QL_TRY(launch_reduce("reduce_xa", ra, st));
-    }
+    g.red_scale = s;
+    g.red_bf16 = reinterpret_cast<__nv_bfloat16*>(XA_save);
+    g.red_bf16_s = reinterpret_cast<__nv_bfloat16*>(XAs);
+    g.red_ld = R;
+    QL_TRY((launch_gemm_red<false, true>("gemm_xa", cdiv(M, 128), 1, 1, splits, tc, mX, mA, g, st)));
   }
 
   // 4. Y = X . Wd^T + (s XA) . B
@@ -685,7 +793,7 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
                                              st)));
     } else {
       dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(N, bn)), 1);
-      QL_TRY((launch_gemm<false, false>("gemm_fwd", grid, tc, mX, mWd, mXAs, mBt, g, st)));
+      QL_TRY((launch_gemm<false, false, EPI_BF16>("gemm_fwd", grid, tc, mX, mWd, mXAs, mBt, g, st)));
     }
   }
   return QLORA_OK;
@@ -717,44 +825,34 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
   uint32_t* err = reinterpret_cast<uint32_t*>(w8 + L.off_err);
   void* WdT = w8 + L.off_wd;
   void* Gs = w8 + L.off_xas;
-  void* XAt = w8 + L.off_xat;
-  void* Gt = w8 + L.off_gt;
-  float* part = reinterpret_cast<float*>(w8 + L.off_part);
+  void* G = w8 + L.off_g;
 
-  CUtensorMap mdY, mB, mWdT, mGs, mA, mXmn, mGt, mdYmn, mXAt;
+  CUtensorMap mdY, mB, mWdT, mGs, mA, mXmn, mGmn, mdYmn, mXAmn;
 
-  // 1. G = dY . B^T per segment (split over the segment's columns)
+  // 1. G = dY . B^T per segment (splits of the segment's columns summed in
+  //    the kernel); writes s*G and G
   {
     const int bn = static_cast<int>(rup(r, 16));
-    const TileCfg tc = tile_cfg(bn);
+    const TileCfg tc = tile_cfg(bn, true);
     const int64_t mt = cdiv(M, 128);
     int64_t min_nkb = INT64_MAX;
     for (int j = 0; j < n_seg; ++j) min_nkb = std::min<int64_t>(min_nkb, cdiv(sg.start[j + 1] - sg.start[j], 64));
-    const int splits = static_cast<int>(std::min<int64_t>(splits_for_rows(min_nkb), min_nkb));
+    const int splits = red_splits<false, false>(mt * n_seg, min_nkb, tc.smem);
     if (!make_map(&mdY, dY, N, M, N, 128) || !make_map(&mB, B, N, r, N, static_cast<uint32_t>(bn)))
       return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(M);
     g.N = r;
     g.mode = GM_G;
-    g.splits = splits;
     g.r = r;
     g.nseg = n_seg;
     for (int j = 0; j <= n_seg; ++j) g.seg_start[j] = sg.start[j];
-    g.out_ld = static_cast<int32_t>(R);
     g.out_valid = r;
-    g.out_split_stride = M * R;
-    g.out = part;
-    QL_TRY((launch_gemm<false, true>("gemm_g", dim3(static_cast<unsigned>(mt), 1, splits * n_seg), tc, mdY, mB, mdY,
-                                     mB, g, st)));
-    {
-      ReduceArgs ra = reduce_args(part, splits, M, R, R, M * R, s);
-      ra.out_bf16_s = reinterpret_cast<__nv_bfloat16*>(Gs);
-      ra.out_bf16_t = reinterpret_cast<__nv_bfloat16*>(Gt);
-      ra.ld_o = R;
-      ra.ld_t = L.Mp;
-      QL_TRY(launch_reduce("reduce_g", ra, st));
-    }
+    g.red_scale = s;
+    g.red_bf16 = reinterpret_cast<__nv_bfloat16*>(G);
+    g.red_bf16_s = reinterpret_cast<__nv_bfloat16*>(Gs);
+    g.red_ld = R;
+    QL_TRY((launch_gemm_red<false, false>("gemm_g", mt, 1, n_seg, splits, tc, mdY, mB, g, st)));
   }
 
   // 2. dX = dY . Wd + (s G) . A^T
@@ -804,71 +902,48 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
       QL_TRY((launch_gemm_pair<true, false>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, mSc, g, st)));
     } else {
       dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(K, bn)), 1);
-      QL_TRY((launch_gemm<false, false>("gemm_dx", grid, tc, mdY, mWdT, mGs, mA, g, st)));
+      QL_TRY((launch_gemm<false, false, EPI_BF16>("gemm_dx", grid, tc, mdY, mWdT, mGs, mA, g, st)));
     }
   }
 
-  // 3. dA = s X^T G   (X read MN-major, split over M)
+  // 3. dA = s X^T G   (X and G read MN-major; splits of M summed in the kernel)
   {
-    const int bn = static_cast<int>(rup(R, 16));
-    const TileCfg tc = tile_cfg(bn);
+    const TileCfg tc = tile_cfg(static_cast<int>(rup(R, 64)), true);
     const int64_t kt = cdiv(K, 128);
-    const int splits = choose_splits(kt, cdiv(M, 64));
-    if (!make_map(&mXmn, X, K, M, K, 64) || !make_map(&mGt, Gt, M, R, L.Mp, static_cast<uint32_t>(bn)))
-      return QLORA_ERR_CUDA;
+    const int splits = red_splits<true, true>(kt, cdiv(M, 64), tc.smem);
+    if (!make_map(&mXmn, X, K, M, K, 64) || !make_map(&mGmn, G, R, M, R, 64)) return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(K);
     g.N = static_cast<int32_t>(R);
     g.mode = GM_PLAIN;
     g.red_len = static_cast<int32_t>(M);
-    g.splits = splits;
-    g.out_ld = static_cast<int32_t>(R);
     g.out_valid = static_cast<int32_t>(R);
-    g.out_split_stride = K * R;
-    g.out = part;
-    QL_TRY((launch_gemm<true, true>("gemm_da", dim3(static_cast<unsigned>(kt), 1, splits), tc, mXmn, mGt, mXmn, mGt,
-                                    g, st)));
-    {
-      ReduceArgs ra = reduce_args(part, splits, K, R, R, K * R, s);
-      ra.out_f32 = dA;
-      ra.ld_o = R;
-      QL_TRY(launch_reduce("reduce_da", ra, st));
-    }
+    g.red_scale = s;
+    g.red_f32 = dA;
+    g.red_ld = R;
+    QL_TRY((launch_gemm_red<true, true>("gemm_da", kt, 1, 1, splits, tc, mXmn, mGmn, g, st)));
   }
 
-  // 4. dB = s XA^T dY  (computed as dB^T = dY^T . XA with dY read MN-major)
+  // 4. dB = s XA^T dY  (computed as dB^T = dY^T . XA with dY and XA read
+  //    MN-major; splits of M summed in the kernel, stored transposed)
   {
-    {
-      const TransposeJob jobs[1] = {tjob(XA_saved, M, R, R, XAt, R, L.Mp, L.Mp)};
-      QL_TRY(launch_transposes("transpose_XA", jobs, 1, st));
-    }
-    const int bn = static_cast<int>(rup(r, 16));
-    const TileCfg tc = tile_cfg(bn);
+    const TileCfg tc = tile_cfg(static_cast<int>(rup(r, 64)), true);
     const int64_t nt = cdiv(N, 128);
-    const int splits = choose_splits(nt, cdiv(M, 64));
-    if (!make_map(&mdYmn, dY, N, M, N, 64) || !make_map(&mXAt, XAt, M, R, L.Mp, static_cast<uint32_t>(bn)))
-      return QLORA_ERR_CUDA;
+    const int splits = red_splits<true, true>(nt, cdiv(M, 64), tc.smem);
+    if (!make_map(&mdYmn, dY, N, M, N, 64) || !make_map(&mXAmn, XA_saved, R, M, R, 64)) return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(N);
     g.N = r;
     g.mode = GM_DB;
     g.red_len = static_cast<int32_t>(M);
-    g.splits = splits;
     g.r = r;
     g.nseg = n_seg;
     for (int j = 0; j <= n_seg; ++j) g.seg_start[j] = sg.start[j];
-    g.out_ld = r;
     g.out_valid = r;
-    g.out_split_stride = N * r;
-    g.out = part;
-    QL_TRY((launch_gemm<true, true>("gemm_db", dim3(static_cast<unsigned>(nt), 1, splits), tc, mdYmn, mXAt, mdYmn,
-                                    mXAt, g, st)));
-    {
-      ReduceArgs ra = reduce_args(part, splits, N, r, r, N * r, s);
-      ra.out_f32_t = dB;
-      ra.ld_t = N;
-      QL_TRY(launch_reduce("reduce_db", ra, st));
-    }
+    g.red_scale = s;
+    g.red_f32_t = dB;
+    g.red_ld_t = N;
+    QL_TRY((launch_gemm_red<true, true>("gemm_db", nt, 1, 1, splits, tc, mdYmn, mXAmn, g, st)));
   }
   return QLORA_OK;
 }
@@ -910,7 +985,7 @@ extern "C" qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t
   if (K % 64 != 0 || K > (int64_t(1) << 30) || M > (int64_t(1) << 30)) return QLORA_ERR_UNSUPPORTED;
   if (!al16(X) || !al16(A) || !al16(XA)) return QLORA_ERR_ALIGNMENT;
   const size_t cap = QLORA_XA_STATIC_SCRATCH_BYTES;
-  const int splits = splits_for_rows(K / 64);
+  const int splits = xa_splits(M, K, R);
   const size_t at_bytes = align256(size_t(R) * K * 2);
   const size_t per_row = size_t(splits) * R * 4;
   if (at_bytes + 128 * per_row > cap) return QLORA_ERR_WORKSPACE;
@@ -947,7 +1022,7 @@ extern "C" qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t
     g.out_valid = R;
     g.out_split_stride = mc * R;
     g.out = part;
-    QL_TRY((launch_gemm<false, true>("gemm_xa_static", dim3(static_cast<unsigned>(cdiv(mc, 128)), 1, splits), tc, mX,
+    QL_TRY((launch_gemm<false, false, EPI_F32_PART>("gemm_xa_static", dim3(static_cast<unsigned>(cdiv(mc, 128)), 1, splits), tc, mX,
                                      mAt, mX, mAt, g, st)));
     ReduceArgs ra = reduce_args(part, splits, mc, R, R, mc * R, 1.0f);
     ra.out_bf16 = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(XA) + size_t(m0) * R * 2);
