@@ -15,10 +15,39 @@ namespace qlora {
 // for odd k.  The fp32 product uses __fmul_rn (IEEE, subnormals kept) and
 // the bf16 rounding is round-to-nearest-even.
 //
-// Each thread converts 8 consecutive weights per step: one 32-bit load of 4
-// packed bytes, one absmax load (8 weights never straddle a 64-block), one
-// 16-byte bf16 store (and two 16-byte fp32 stores when requested).  A warp
-// thus reads 128 contiguous bytes and writes 512 contiguous bytes.
+// A group is 8 consecutive weights: one 32-bit word of 4 packed bytes, one
+// absmax (8 weights never straddle a 64-block), one 16-byte bf16 store (and
+// two 16-byte fp32 stores when requested).  A warp takes chunks of 4 x 32
+// consecutive groups; lane l converts groups l, 32+l, 64+l, 96+l of its
+// chunk, issuing the four loads before any arithmetic so that four are in
+// flight, and each of its stores is one contiguous 512-byte warp store.
+__device__ __forceinline__ void dequant_group(uint32_t packed, float am, const float* cb, int64_t g,
+                                              uint4* __restrict__ out_bf16, float4* __restrict__ out_f32) {
+  float w[8];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t byte = (packed >> (8 * b)) & 0xFFu;
+    w[2 * b] = __fmul_rn(cb[byte & 0xFu], am);
+    w[2 * b + 1] = __fmul_rn(cb[byte >> 4], am);
+  }
+  if (out_bf16) {
+    uint4 o;
+    __nv_bfloat162 h0 = __floats2bfloat162_rn(w[0], w[1]);
+    __nv_bfloat162 h1 = __floats2bfloat162_rn(w[2], w[3]);
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(w[4], w[5]);
+    __nv_bfloat162 h3 = __floats2bfloat162_rn(w[6], w[7]);
+    o.x = *reinterpret_cast<uint32_t*>(&h0);
+    o.y = *reinterpret_cast<uint32_t*>(&h1);
+    o.z = *reinterpret_cast<uint32_t*>(&h2);
+    o.w = *reinterpret_cast<uint32_t*>(&h3);
+    out_bf16[g] = o;
+  }
+  if (out_f32) {
+    out_f32[2 * g] = make_float4(w[0], w[1], w[2], w[3]);
+    out_f32[2 * g + 1] = make_float4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 __global__ void __launch_bounds__(256) dequant4_kernel(const uint32_t* __restrict__ idx4,
                                                        const float* __restrict__ absmax,
                                                        const float* __restrict__ codebook, int64_t n_groups,
@@ -29,32 +58,24 @@ __global__ void __launch_bounds__(256) dequant4_kernel(const uint32_t* __restric
   griddep_launch_dependents();
   if (threadIdx.x < 16) cb[threadIdx.x] = codebook[threadIdx.x];
   __syncthreads();
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < n_groups; g += stride) {
-    const uint32_t packed = __ldg(idx4 + g);
-    const float am = __ldg(absmax + (g >> 3));  // 8 groups of 8 weights per 64-block
-    float w[8];
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t chunks = (n_groups + 127) / 128;
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); c < chunks;
+       c += warps) {
+    const int64_t g0 = c * 128 + lane;
+    uint32_t packed[4];
+    float am[4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t byte = (packed >> (8 * b)) & 0xFFu;
-      w[2 * b] = __fmul_rn(cb[byte & 0xFu], am);
-      w[2 * b + 1] = __fmul_rn(cb[byte >> 4], am);
+    for (int i = 0; i < 4; ++i) {
+      const int64_t g = g0 + 32 * i;
+      packed[i] = g < n_groups ? __ldg(idx4 + g) : 0u;
+      am[i] = g < n_groups ? __ldg(absmax + (g >> 3)) : 0.f;  // 8 groups per 64-block
     }
-    if (out_bf16) {
-      uint4 o;
-      __nv_bfloat162 h0 = __floats2bfloat162_rn(w[0], w[1]);
-      __nv_bfloat162 h1 = __floats2bfloat162_rn(w[2], w[3]);
-      __nv_bfloat162 h2 = __floats2bfloat162_rn(w[4], w[5]);
-      __nv_bfloat162 h3 = __floats2bfloat162_rn(w[6], w[7]);
-      o.x = *reinterpret_cast<uint32_t*>(&h0);
-      o.y = *reinterpret_cast<uint32_t*>(&h1);
-      o.z = *reinterpret_cast<uint32_t*>(&h2);
-      o.w = *reinterpret_cast<uint32_t*>(&h3);
-      out_bf16[g] = o;
-    }
-    if (out_f32) {
-      out_f32[2 * g] = make_float4(w[0], w[1], w[2], w[3]);
-      out_f32[2 * g + 1] = make_float4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t g = g0 + 32 * i;
+      if (g < n_groups) dequant_group(packed[i], am[i], cb, g, out_bf16, out_f32);
     }
   }
 }

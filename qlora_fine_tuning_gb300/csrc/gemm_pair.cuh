@@ -96,6 +96,8 @@ __device__ __forceinline__ void pair_tile_coords(const GemmArgs& p, int tile, in
 
 // B_MN: B is read MN-major (its rows are reduction rows holding 64 output
 // columns each; used for dX straight from the row-major dequantised weight).
+// The rank-r steps read B2 the other way round: MN-major in the forward
+// (B [r,N] as stored), K-major for dX (A [K,R] as stored).
 // With FUSED_DQ, tmB maps the packed codes (uint8 [N, K/2]) and tmS the
 // absmax (fp32 [N, K/64]); otherwise tmB maps the bf16 B operand and tmS is
 // unused.
@@ -105,6 +107,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192
                      const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                      const __grid_constant__ CUtensorMap tmS, const GemmArgs p) {
   constexpr uint32_t kStage = FUSED_DQ ? kPairDqStageBytes : kPairStageBytes;
+  // The rank-r B-operand is read MN-major exactly when the main one is not:
+  // forward B2 = B [r,N] (rows = rank index), dX B2 = A [K,R] (rows = output).
+  constexpr bool B2_MN = !B_MN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((((raw + 1023u) & ~1023u)) - raw);
@@ -252,7 +257,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192
         } else {
           const int a = it - nkb;
           tma_load_2d_pair_ws(a_dst, &tmA2, bar, a2_x0 + 64 * a, m0);
-          tma_load_2d_pair_ws(b_dst, &tmB2, bar, 64 * a, n0);
+          if (B2_MN) {
+            tma_load_2d_pair_ws(b_dst, &tmB2, bar, n0, 64 * a);
+            tma_load_2d_pair_ws(b_dst + 8192, &tmB2, bar, n0 + 64, 64 * a);
+          } else {
+            tma_load_2d_pair_ws(b_dst, &tmB2, bar, 64 * a, n0);
+          }
         }
         ++g;
       }
@@ -269,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192
     // ---------------- MMA issuer (even CTA; whole warp, elected lane issues) ----------------
     if (rank == 0) {
       const uint32_t idesc = idesc_bf16_f32(256, 256, false, B_MN);
-      const uint32_t idesc_lora = idesc_bf16_f32(256, 256, false, false);
+      const uint32_t idesc_lora = idesc_bf16_f32(256, 256, false, B2_MN);
       uint32_t g = 0;
       int j = 0;
       bool ok = true;
@@ -307,8 +317,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192
             const int ksteps = min(4, p.lora_ksteps - 4 * (it - nkb));
             for (int kk = 0; kk < ksteps; ++kk)
               tc_mma_bf16_pair_ws(d_tmem, sdesc_sw128(a_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u),
-                                  sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u), idesc_lora,
-                                  (it > 0 || kk > 0) ? 1u : 0u);
+                                  B2_MN ? sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 2048u, 8192u, 1024u)
+                                        : sdesc_sw128(b_addr + static_cast<uint32_t>(kk) * 32u, 16u, 1024u),
+                                  idesc_lora, (it > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit_pair_multicast_ws(&empty[s], 0x3);
           ++g;

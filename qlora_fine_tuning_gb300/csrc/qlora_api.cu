@@ -542,7 +542,7 @@ GemmArgs base_args(uint32_t* err) {
 qlora_status launch_dequant(const qlora_w4* w, void* out_bf16, float* out_f32, cudaStream_t st) {
   const int64_t groups = w->N * w->K / 8;
   if (groups == 0) return QLORA_OK;
-  const int64_t blocks = std::min<int64_t>(cdiv(groups, 256), int64_t(kSMs) * 16);
+  const int64_t blocks = std::min<int64_t>(cdiv(groups, 1024), int64_t(kSMs) * 8);  // 8 warps x 128 groups
   LaunchScope ls("dequant4", st);
   return cuda_status(launch_k(dequant4_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
                               reinterpret_cast<const uint32_t*>(w->idx), w->absmax, w->codebook, groups,
@@ -723,18 +723,20 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
   void* XAs = w8 + L.off_xas;
   const int64_t R = L.R;
 
-  // 1. Wd = deq(W), unless the pair GEMM dequantises in shared memory
+  // 1. B^T [N,Rp] (zero columns r..Rp-1): the rank-r B-operand of the
+  //    single-CTA Y GEMM (the CTA-pair kernel reads B [r,N] MN-major)
   bool b256 = true;
   for (int j = 1; j < n_seg; ++j)
     if (sg.start[j] % 256 != 0) b256 = false;
   const bool pair_fwd = b256 && pair_enabled();
-  const bool fused_fwd = pair_fwd && fused_dq_ok(W);
-  if (!fused_fwd) QL_TRY(launch_dequant(W, Wd, nullptr, st));
-  // 2. B^T [N,Rp] (zero columns r..Rp-1): the LoRA B-operand of the Y GEMM
-  {
+  if (!pair_fwd) {
     const TransposeJob jobs[1] = {tjob(B, r, N, N, Bt, N, L.Rp, L.Rp)};
     QL_TRY(launch_transposes("transpose_B", jobs, 1, st));
   }
+
+  // 2. Wd = deq(W), unless the pair GEMM dequantises in shared memory
+  const bool fused_fwd = pair_fwd && fused_dq_ok(W);
+  if (!fused_fwd) QL_TRY(launch_dequant(W, Wd, nullptr, st));
 
   // 3. XA = X . A (A read MN-major; splits of K summed in the kernel);
   //    writes XA_save = bf16(XA) and s*XA
@@ -770,7 +772,8 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
       if (!make_map(&mWd, Wd, K, N, K, brows)) return QLORA_ERR_CUDA;
       mSc = mWd;
     }
-    if (!make_map(&mXAs, XAs, R, M, R, 128) || !make_map(&mBt, Bt, L.Rp, N, L.Rp, brows)) return QLORA_ERR_CUDA;
+    if (!make_map(&mXAs, XAs, R, M, R, 128)) return QLORA_ERR_CUDA;
+    if (pair ? !make_map(&mBt, B, N, r, N, 64) : !make_map(&mBt, Bt, L.Rp, N, L.Rp, brows)) return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(M);
     g.N = static_cast<int32_t>(N);
