@@ -307,12 +307,13 @@ constexpr int kSmemLimit = 232448;
 
 // Launches may overlap the tail of their predecessor in the stream
 // (programmatic dependent launch; each kernel waits with griddepcontrol.wait
-// before it touches global memory).  Off by default: on GB300 it measured
-// about 1% slower for the MLP step.  QLORA_ENABLE_PDL=1 turns it on.
+// before it touches global memory, so the overlap covers only its prologue:
+// barrier set-up, tensor-memory allocation, descriptor prefetch).  On by
+// default; QLORA_PDL=0 turns it off.
 bool pdl_enabled() {
   static const bool on = [] {
-    const char* e = std::getenv("QLORA_ENABLE_PDL");
-    return e && e[0] == '1';
+    const char* e = std::getenv("QLORA_PDL");
+    return !(e && e[0] == '0');
   }();
   return on;
 }
