@@ -183,7 +183,7 @@ template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
-                   const GemmArgs p) {
+                   const __grid_constant__ GemmArgs p, const __grid_constant__ GemmArgs p2) {
   constexpr bool RED = (EPI == EPI_RED);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -208,10 +208,15 @@ __global__ void __launch_bounds__(192, 1)
   // Tile walk: CTAs (or clusters) take every stride-th tile.
   const int walk_first = RED ? static_cast<int>(blockIdx.x) / S : static_cast<int>(blockIdx.x);
   const int walk_stride = RED ? static_cast<int>(gridDim.x) / S : static_cast<int>(gridDim.x);
-  const int walk_total = RED ? total / S : total;
+  // EPI_RED may carry a second, independent problem `p2` (its own tensor maps
+  // in the tmA2 / tmB2 slots, which rank-r GEMMs do not otherwise use): the
+  // walk covers p's tiles, then p2's.  p2.m_tiles == 0 means none.
+  const int tiles1 = RED ? total / S : total;
+  const int tiles2 = RED ? p2.m_tiles * p2.n_tiles * (p2.z_tiles / S) : 0;
+  const int walk_total = tiles1 + tiles2;
   const bool has_lora = (p.mode == GM_FWD || p.mode == GM_DX) && p.lora_atoms > 0;
   uint32_t acc_cols = 32;
-  while (acc_cols < static_cast<uint32_t>(p.bn)) acc_cols <<= 1;
+  while (acc_cols < static_cast<uint32_t>(max(p.bn, tiles2 > 0 ? p2.bn : 0))) acc_cols <<= 1;
   const uint32_t tmem_cols = 2 * acc_cols;
 
   if (threadIdx.x == 0) {
@@ -238,7 +243,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 1 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (has_lora) {
+    if (has_lora || tiles2 > 0) {
       tma_prefetch_desc(&tmA2);
       tma_prefetch_desc(&tmB2);
     }
@@ -255,11 +260,15 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
-    const uint32_t tx = kATileBytes + static_cast<uint32_t>(p.bn) * 128u;
     uint32_t g = 0;  // iterations issued so far (ring position)
     bool ok = true;
     for (int T = walk_first; T < walk_total && ok; T += walk_stride) {
-      const TileInfo t = tile_info(p, RED ? red_tile(p, T, rank) : T);
+      const bool second = T >= tiles1;
+      const GemmArgs& pq = second ? p2 : p;
+      const CUtensorMap* mapA = second ? &tmA2 : &tmA;
+      const CUtensorMap* mapB = second ? &tmB2 : &tmB;
+      const TileInfo t = tile_info(pq, RED ? red_tile(pq, second ? T - tiles1 : T, rank) : T);
+      const uint32_t tx = kATileBytes + static_cast<uint32_t>(pq.bn) * 128u;
       for (int it = 0; it < t.n_iter; ++it) {
         const uint32_t s = g % static_cast<uint32_t>(p.stages);
         const uint32_t ph = (g / static_cast<uint32_t>(p.stages)) & 1u;
@@ -281,16 +290,16 @@ __global__ void __launch_bounds__(192, 1)
         if (it < t.n_main) {
           const int kel = t.red_begin + (t.kb0 + it) * 64;
           if (A_MN) {
-            tma_load_2d_ws(a_dst, &tmA, &full[s], t.m0, kel);
-            tma_load_2d_ws(a_dst + 8192, &tmA, &full[s], t.m0 + 64, kel);
+            tma_load_2d_ws(a_dst, mapA, &full[s], t.m0, kel);
+            tma_load_2d_ws(a_dst + 8192, mapA, &full[s], t.m0 + 64, kel);
           } else {
-            tma_load_2d_ws(a_dst, &tmA, &full[s], kel, t.m0);
+            tma_load_2d_ws(a_dst, mapA, &full[s], kel, t.m0);
           }
           if (B_MN) {
-            for (int i = 0; i < p.bn / 64; ++i)
-              tma_load_2d_ws(b_dst + i * 8192, &tmB, &full[s], t.b_row0 + 64 * i, kel);
+            for (int i = 0; i < pq.bn / 64; ++i)
+              tma_load_2d_ws(b_dst + i * 8192, mapB, &full[s], t.b_row0 + 64 * i, kel);
           } else {
-            tma_load_2d_ws(b_dst, &tmB, &full[s], kel, t.b_row0);
+            tma_load_2d_ws(b_dst, mapB, &full[s], kel, t.b_row0);
           }
         } else {
           const int a = it - t.n_main;
@@ -308,7 +317,6 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
-    const uint32_t idesc_main = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), A_MN, B_MN);
     const uint32_t idesc_lora = idesc_bf16_f32(128, static_cast<uint32_t>(p.bn), false, false);
     const uint64_t a_step = A_MN ? (2048u >> 4) : (32u >> 4);
     const uint64_t b_step = B_MN ? (2048u >> 4) : (32u >> 4);
@@ -316,7 +324,10 @@ __global__ void __launch_bounds__(192, 1)
     int j = 0;
     bool ok = true;
     for (int T = walk_first; T < walk_total && ok; T += walk_stride, ++j) {
-      const TileInfo t = tile_info(p, RED ? red_tile(p, T, rank) : T);
+      const bool second = T >= tiles1;
+      const GemmArgs& pq = second ? p2 : p;
+      const TileInfo t = tile_info(pq, RED ? red_tile(pq, second ? T - tiles1 : T, rank) : T);
+      const uint32_t idesc_main = idesc_bf16_f32(128, static_cast<uint32_t>(pq.bn), A_MN, B_MN);
       const uint32_t acc = static_cast<uint32_t>(j & 1);
       if (!warp_wait(&tempty[acc], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
         if (lane == 0) {
@@ -375,7 +386,9 @@ __global__ void __launch_bounds__(192, 1)
     int j = 0;
     bool ok = true;
     for (int T = walk_first; T < walk_total && ok; T += walk_stride, ++j) {
-      const TileInfo t = tile_info(p, red_tile(p, T, rank));
+      const bool second = T >= tiles1;
+      const GemmArgs& pq = second ? p2 : p;
+      const TileInfo t = tile_info(pq, red_tile(pq, second ? T - tiles1 : T, rank));
       const uint32_t acc = static_cast<uint32_t>(j & 1);
       if (!warp_wait(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
         if (lane == 0) {
@@ -389,7 +402,7 @@ __global__ void __launch_bounds__(192, 1)
       if (S == 1) {
         // One split: the accumulator is the sum; store straight from registers.
         const int grow = t.m0 + row;
-        for (int c = 0; c < p.bn; c += 16) {
+        for (int c = 0; c < pq.bn; c += 16) {
           uint32_t v[16];
           if (t.n_iter > 0) {
             tmem_ld16(t_base + static_cast<uint32_t>(c), v);
@@ -398,40 +411,40 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = 0u;
           }
-          if (grow >= p.M) continue;
+          if (grow >= pq.M) continue;
           const int gcol = t.n0 + c;
-          const int lim = min(p.out_valid, p.N);
-          if (p.red_f32_t) {
+          const int lim = min(pq.out_valid, pq.N);
+          if (pq.red_f32_t) {
             // a warp's 32 rows are 32 consecutive outputs of each column
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               if (gcol + e < lim)
-                p.red_f32_t[static_cast<int64_t>(gcol + e + t.out_col0) * p.red_ld_t + grow] =
-                    __fmul_rn(p.red_scale, __uint_as_float(v[e]));
+                pq.red_f32_t[static_cast<int64_t>(gcol + e + t.out_col0) * pq.red_ld_t + grow] =
+                    __fmul_rn(pq.red_scale, __uint_as_float(v[e]));
           } else {
-            const int64_t o = static_cast<int64_t>(grow) * p.red_ld + t.out_col0 + gcol;
+            const int64_t o = static_cast<int64_t>(grow) * pq.red_ld + t.out_col0 + gcol;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if (gcol + 8 * h >= lim) continue;
               const float* f = reinterpret_cast<const float*>(v) + 8 * h;
-              if (p.red_bf16)
-                *reinterpret_cast<uint4*>(p.red_bf16 + o + 8 * h) =
+              if (pq.red_bf16)
+                *reinterpret_cast<uint4*>(pq.red_bf16 + o + 8 * h) =
                     make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
                                pack_bf16x2(f[6], f[7]));
-              if (p.red_bf16_s) {
+              if (pq.red_bf16_s) {
                 float g8[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) g8[e] = __fmul_rn(p.red_scale, f[e]);
-                *reinterpret_cast<uint4*>(p.red_bf16_s + o + 8 * h) =
+                for (int e = 0; e < 8; ++e) g8[e] = __fmul_rn(pq.red_scale, f[e]);
+                *reinterpret_cast<uint4*>(pq.red_bf16_s + o + 8 * h) =
                     make_uint4(pack_bf16x2(g8[0], g8[1]), pack_bf16x2(g8[2], g8[3]), pack_bf16x2(g8[4], g8[5]),
                                pack_bf16x2(g8[6], g8[7]));
               }
-              if (p.red_f32) {
+              if (pq.red_f32) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e)
-                  *reinterpret_cast<float4*>(p.red_f32 + o + 8 * h + 4 * e) =
-                      make_float4(__fmul_rn(p.red_scale, f[4 * e]), __fmul_rn(p.red_scale, f[4 * e + 1]),
-                                  __fmul_rn(p.red_scale, f[4 * e + 2]), __fmul_rn(p.red_scale, f[4 * e + 3]));
+                  *reinterpret_cast<float4*>(pq.red_f32 + o + 8 * h + 4 * e) =
+                      make_float4(__fmul_rn(pq.red_scale, f[4 * e]), __fmul_rn(pq.red_scale, f[4 * e + 1]),
+                                  __fmul_rn(pq.red_scale, f[4 * e + 2]), __fmul_rn(pq.red_scale, f[4 * e + 3]));
               }
             }
           }
@@ -441,8 +454,8 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) mbar_arrive(&tempty[acc]);
         continue;
       }
-      for (int c64 = 0; c64 < p.bn; c64 += 64, ++round) {
-        const int cw = min(64, p.bn - c64);
+      for (int c64 = 0; c64 < pq.bn; c64 += 64, ++round) {
+        const int cw = min(64, pq.bn - c64);
         // 1. this CTA's buffer has been read by every CTA in the previous round
         if (!warp_wait_cluster(red_free, (round & 1u) ^ 1u, p.timeout_ns, abort_flag)) {
           ok = false;
@@ -464,7 +477,7 @@ __global__ void __launch_bounds__(192, 1)
             dst[e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
                                  __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
         }
-        if (c64 + 64 >= p.bn) {  // accumulator read out: the MMA warp may reuse it
+        if (c64 + 64 >= pq.bn) {  // accumulator read out: the MMA warp may reuse it
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -484,7 +497,7 @@ __global__ void __launch_bounds__(192, 1)
         constexpr int kB = 4;
         const int g4 = cw / 4;
         const int items = nrows * g4;
-        const bool tr = p.red_f32_t != nullptr;
+        const bool tr = pq.red_f32_t != nullptr;
         for (int base = et; base < items; base += 128 * kB) {
           uint32_t off[kB];
           int rr[kB], cc[kB];
@@ -513,26 +526,26 @@ __global__ void __launch_bounds__(192, 1)
           for (int i = 0; i < kB; ++i) {
             if (base + 128 * i >= items) break;
             const int grow = t.m0 + rr[i], gcol = t.n0 + c64 + cc[i];
-            if (grow >= p.M || gcol >= p.out_valid || gcol >= p.N) continue;
+            if (grow >= pq.M || gcol >= pq.out_valid || gcol >= pq.N) continue;
             const float f[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
             if (tr) {
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                p.red_f32_t[static_cast<int64_t>(gcol + e + t.out_col0) * p.red_ld_t + grow] =
-                    __fmul_rn(p.red_scale, f[e]);
+                pq.red_f32_t[static_cast<int64_t>(gcol + e + t.out_col0) * pq.red_ld_t + grow] =
+                    __fmul_rn(pq.red_scale, f[e]);
               continue;
             }
-            const int64_t o = static_cast<int64_t>(grow) * p.red_ld + t.out_col0 + gcol;
-            if (p.red_bf16)
-              *reinterpret_cast<uint2*>(p.red_bf16 + o) = make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
-            if (p.red_bf16_s)
-              *reinterpret_cast<uint2*>(p.red_bf16_s + o) =
-                  make_uint2(pack_bf16x2(__fmul_rn(p.red_scale, f[0]), __fmul_rn(p.red_scale, f[1])),
-                             pack_bf16x2(__fmul_rn(p.red_scale, f[2]), __fmul_rn(p.red_scale, f[3])));
-            if (p.red_f32)
-              *reinterpret_cast<float4*>(p.red_f32 + o) =
-                  make_float4(__fmul_rn(p.red_scale, f[0]), __fmul_rn(p.red_scale, f[1]),
-                              __fmul_rn(p.red_scale, f[2]), __fmul_rn(p.red_scale, f[3]));
+            const int64_t o = static_cast<int64_t>(grow) * pq.red_ld + t.out_col0 + gcol;
+            if (pq.red_bf16)
+              *reinterpret_cast<uint2*>(pq.red_bf16 + o) = make_uint2(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]));
+            if (pq.red_bf16_s)
+              *reinterpret_cast<uint2*>(pq.red_bf16_s + o) =
+                  make_uint2(pack_bf16x2(__fmul_rn(pq.red_scale, f[0]), __fmul_rn(pq.red_scale, f[1])),
+                             pack_bf16x2(__fmul_rn(pq.red_scale, f[2]), __fmul_rn(pq.red_scale, f[3])));
+            if (pq.red_f32)
+              *reinterpret_cast<float4*>(pq.red_f32 + o) =
+                  make_float4(__fmul_rn(pq.red_scale, f[0]), __fmul_rn(pq.red_scale, f[1]),
+                              __fmul_rn(pq.red_scale, f[2]), __fmul_rn(pq.red_scale, f[3]));
           }
         }
         // 6. done reading this round: arrive (release) on every CTA's red_free

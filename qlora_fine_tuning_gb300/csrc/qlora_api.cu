@@ -375,7 +375,9 @@ qlora_status launch_gemm(const char* name, dim3 grid, const TileCfg& tc, const C
   cudaError_t e;
   {
     LaunchScope ls(name, st);
-    e = launch_k(gemm_tc_kernel<A_MN, B_MN, EPI>, dim3(ctas), dim3(192), tc.smem, st, a, b, a2, b2, args);
+    GemmArgs none;
+    std::memset(&none, 0, sizeof(none));
+    e = launch_k(gemm_tc_kernel<A_MN, B_MN, EPI>, dim3(ctas), dim3(192), tc.smem, st, a, b, a2, b2, args, none);
   }
   return cuda_status(e);
 }
@@ -426,11 +428,19 @@ int red_splits(int64_t tiles, int64_t nkb, size_t smem) {
   return 1;
 }
 
-// gemm_tc_kernel<.., EPI_RED>: tiles m_tiles x n_tiles x zseg (zseg adapter
-// segments for GM_G, else 1), `splits` CTAs per tile in one cluster.
+// One problem of a gemm_tc_kernel<.., EPI_RED> launch: tiles m_tiles x
+// n_tiles x zseg (zseg adapter segments for GM_G, else 1).
+struct RedProb {
+  GemmArgs g;
+  CUtensorMap a, b;
+  int64_t m_tiles, n_tiles, zseg;
+  int bn;
+};
+
+// gemm_tc_kernel<.., EPI_RED>: `splits` CTAs per tile in one cluster; an
+// optional second problem shares the launch (its tiles follow the first's).
 template <bool A_MN, bool B_MN>
-qlora_status launch_gemm_red(const char* name, int64_t m_tiles, int64_t n_tiles, int64_t zseg, int splits,
-                             const TileCfg& tc, const CUtensorMap& a, const CUtensorMap& b, GemmArgs args,
+qlora_status launch_gemm_red(const char* name, int splits, const TileCfg& tc, RedProb p1, const RedProb* p2,
                              cudaStream_t st) {
   auto kern = gemm_tc_kernel<A_MN, B_MN, EPI_RED>;
   static std::once_flag attr_once[64];
@@ -439,17 +449,30 @@ qlora_status launch_gemm_red(const char* name, int64_t m_tiles, int64_t n_tiles,
   std::call_once(attr_once[dev & 63], [kern] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   });
-  args.bn = tc.bn;
-  args.stages = tc.stages;
-  args.stage_bytes = tc.stage_bytes;
-  args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-  args.debug_stall = take_stall(name) ? 1 : 0;
-  args.l2_hints = 0;
-  args.splits = splits;
-  args.m_tiles = static_cast<int32_t>(m_tiles);
-  args.n_tiles = static_cast<int32_t>(n_tiles);
-  args.z_tiles = static_cast<int32_t>(zseg * splits);
-  const int64_t tiles = m_tiles * n_tiles * zseg;
+  auto fill = [&](RedProb& pr) {
+    GemmArgs& a = pr.g;
+    a.bn = pr.bn;
+    a.stages = tc.stages;
+    a.stage_bytes = tc.stage_bytes;
+    a.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    a.l2_hints = 0;
+    a.splits = splits;
+    a.m_tiles = static_cast<int32_t>(pr.m_tiles);
+    a.n_tiles = static_cast<int32_t>(pr.n_tiles);
+    a.z_tiles = static_cast<int32_t>(pr.zseg * splits);
+  };
+  fill(p1);
+  p1.g.debug_stall = take_stall(name) ? 1 : 0;
+  RedProb q2;
+  if (p2) {
+    q2 = *p2;
+    fill(q2);
+  } else {
+    std::memset(&q2.g, 0, sizeof(q2.g));
+    q2.a = p1.a;
+    q2.b = p1.b;
+  }
+  const int64_t tiles = p1.m_tiles * p1.n_tiles * p1.zseg + (p2 ? p2->m_tiles * p2->n_tiles * p2->zseg : 0);
   const int64_t clusters = std::min<int64_t>(tiles, max_red_clusters<A_MN, B_MN>(splits, tc.smem));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * splits));
@@ -468,7 +491,7 @@ qlora_status launch_gemm_red(const char* name, int64_t m_tiles, int64_t n_tiles,
   cudaError_t e;
   {
     LaunchScope ls(name, st);
-    e = cudaLaunchKernelEx(&cfg, kern, a, b, a, b, args);
+    e = cudaLaunchKernelEx(&cfg, kern, p1.a, p1.b, q2.a, q2.b, p1.g, q2.g);
   }
   return cuda_status(e);
 }
@@ -757,7 +780,8 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     g.red_bf16 = reinterpret_cast<__nv_bfloat16*>(XA_save);
     g.red_bf16_s = reinterpret_cast<__nv_bfloat16*>(XAs);
     g.red_ld = R;
-    QL_TRY((launch_gemm_red<false, true>("gemm_xa", cdiv(M, 128), 1, 1, splits, tc, mX, mA, g, st)));
+    QL_TRY((launch_gemm_red<false, true>("gemm_xa", splits, tc, RedProb{g, mX, mA, cdiv(M, 128), 1, 1, tc.bn},
+                                         nullptr, st)));
   }
 
   // 4. Y = X . Wd^T + (s XA) . B
@@ -856,7 +880,8 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     g.red_bf16 = reinterpret_cast<__nv_bfloat16*>(G);
     g.red_bf16_s = reinterpret_cast<__nv_bfloat16*>(Gs);
     g.red_ld = R;
-    QL_TRY((launch_gemm_red<false, false>("gemm_g", mt, 1, n_seg, splits, tc, mdY, mB, g, st)));
+    QL_TRY((launch_gemm_red<false, false>("gemm_g", splits, tc, RedProb{g, mdY, mB, mt, 1, n_seg, bn}, nullptr,
+                                          st)));
   }
 
   // 2. dX = dY . Wd + (s G) . A^T
@@ -910,44 +935,43 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     }
   }
 
-  // 3. dA = s X^T G   (X and G read MN-major; splits of M summed in the kernel)
+  // 3+4. dA = s X^T G and dB = s XA^T dY in one launch (both reduce over the
+  //    M tokens and read every operand MN-major; splits of M summed in the
+  //    kernel).  dB is computed as dB^T = dY^T . XA and stored transposed.
+  //    A dA tile streams 128 columns of X, a dB tile 128 columns of dY: the
+  //    tiles of the two problems are the same amount of work.
   {
-    const TileCfg tc = tile_cfg(static_cast<int>(rup(R, 64)), true);
-    const int64_t kt = cdiv(K, 128);
-    const int splits = red_splits<true, true>(kt, cdiv(M, 64), tc.smem);
-    if (!make_map(&mXmn, X, K, M, K, 64) || !make_map(&mGmn, G, R, M, R, 64)) return QLORA_ERR_CUDA;
-    GemmArgs g = base_args(err);
-    g.M = static_cast<int32_t>(K);
-    g.N = static_cast<int32_t>(R);
-    g.mode = GM_PLAIN;
-    g.red_len = static_cast<int32_t>(M);
-    g.out_valid = static_cast<int32_t>(R);
-    g.red_scale = s;
-    g.red_f32 = dA;
-    g.red_ld = R;
-    QL_TRY((launch_gemm_red<true, true>("gemm_da", kt, 1, 1, splits, tc, mXmn, mGmn, g, st)));
-  }
-
-  // 4. dB = s XA^T dY  (computed as dB^T = dY^T . XA with dY and XA read
-  //    MN-major; splits of M summed in the kernel, stored transposed)
-  {
-    const TileCfg tc = tile_cfg(static_cast<int>(rup(r, 64)), true);
-    const int64_t nt = cdiv(N, 128);
-    const int splits = red_splits<true, true>(nt, cdiv(M, 64), tc.smem);
-    if (!make_map(&mdYmn, dY, N, M, N, 64) || !make_map(&mXAmn, XA_saved, R, M, R, 64)) return QLORA_ERR_CUDA;
-    GemmArgs g = base_args(err);
-    g.M = static_cast<int32_t>(N);
-    g.N = r;
-    g.mode = GM_DB;
-    g.red_len = static_cast<int32_t>(M);
-    g.r = r;
-    g.nseg = n_seg;
-    for (int j = 0; j <= n_seg; ++j) g.seg_start[j] = sg.start[j];
-    g.out_valid = r;
-    g.red_scale = s;
-    g.red_f32_t = dB;
-    g.red_ld_t = N;
-    QL_TRY((launch_gemm_red<true, true>("gemm_db", nt, 1, 1, splits, tc, mdYmn, mXAmn, g, st)));
+    const int bn_a = static_cast<int>(rup(R, 64)), bn_b = static_cast<int>(rup(r, 64));
+    const TileCfg tc = tile_cfg(std::max(bn_a, bn_b), true);
+    const int64_t kt = cdiv(K, 128), nt = cdiv(N, 128);
+    const int splits = red_splits<true, true>(kt + nt, cdiv(M, 64), tc.smem);
+    if (!make_map(&mXmn, X, K, M, K, 64) || !make_map(&mGmn, G, R, M, R, 64) ||
+        !make_map(&mdYmn, dY, N, M, N, 64) || !make_map(&mXAmn, XA_saved, R, M, R, 64))
+      return QLORA_ERR_CUDA;
+    GemmArgs ga = base_args(err);
+    ga.M = static_cast<int32_t>(K);
+    ga.N = static_cast<int32_t>(R);
+    ga.mode = GM_PLAIN;
+    ga.red_len = static_cast<int32_t>(M);
+    ga.out_valid = static_cast<int32_t>(R);
+    ga.red_scale = s;
+    ga.red_f32 = dA;
+    ga.red_ld = R;
+    GemmArgs gb = base_args(err);
+    gb.M = static_cast<int32_t>(N);
+    gb.N = r;
+    gb.mode = GM_DB;
+    gb.red_len = static_cast<int32_t>(M);
+    gb.r = r;
+    gb.nseg = n_seg;
+    for (int j = 0; j <= n_seg; ++j) gb.seg_start[j] = sg.start[j];
+    gb.out_valid = r;
+    gb.red_scale = s;
+    gb.red_f32_t = dB;
+    gb.red_ld_t = N;
+    const RedProb pb{gb, mdYmn, mXAmn, nt, 1, 1, bn_b};
+    QL_TRY((launch_gemm_red<true, true>("gemm_dadb", splits, tc, RedProb{ga, mXmn, mGmn, kt, 1, 1, bn_a}, &pb,
+                                        st)));
   }
   return QLORA_OK;
 }

@@ -21,7 +21,7 @@ def _short_waits():
     binding.qlora_set_wait_limit_ns(2_000_000_000)
 
 
-@pytest.mark.parametrize("label", ["gemm_xa", "gemm_fwd", "gemm_g", "gemm_dx", "gemm_db"])
+@pytest.mark.parametrize("label", ["gemm_xa", "gemm_fwd", "gemm_g", "gemm_dx", "gemm_dadb"])
 def test_stalled_pipeline_reports_timeout_and_next_call_is_correct(label):
     li = synth.make_linear(256, 512, 512, 16, 1.0, seed=77)
     g = GpuLayer(li)
