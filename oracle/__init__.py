@@ -58,6 +58,8 @@ def _load():
             lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
             lib.oracle_dequant.restype = None
             lib.oracle_dequant.argtypes = [P, P, P, I, I, I, P, P]
+            lib.oracle_quantize.restype = None
+            lib.oracle_quantize.argtypes = [P, I, I, I, P, P, P]
             lib.oracle_forward_rows.restype = None
             lib.oracle_forward_rows.argtypes = [P, P, P, P, I, I, I, I, I, P, D, P, I, P, P]
             lib.oracle_backward_dx_rows.restype = None
@@ -120,6 +122,24 @@ def dequant(idx, absmax, codebook, N: int, K: int, block: int = 64):
     w16 = np.empty((N, K), dtype=np.uint16)
     lib.oracle_dequant(_p(idx), _p(absmax), _p(codebook), N, K, block, _p(w32), _p(w16))
     return w32, w16
+
+
+def quantize(w, codebook, block: int = 64):
+    """fp32 W [N,K] -> (idx uint8 [N,K/2], absmax float32 [N*K/block]).
+
+    Per block of the row-major flattening: absmax = max |w|; the code of each
+    element is the first i minimising |w/absmax - codebook[i]| in double
+    precision (t = 0 for a zero block).  Pass bf16 weights widened to fp32.
+    """
+    lib = _load()
+    w = _c(w, np.float32)
+    codebook = _c(codebook, np.float32)
+    N, K = w.shape
+    assert K % block == 0 and codebook.size == 16
+    idx = np.empty((N, K // 2), dtype=np.uint8)
+    absmax = np.empty((N * K // block,), dtype=np.float32)
+    lib.oracle_quantize(_p(w), N, K, block, _p(codebook), _p(idx), _p(absmax))
+    return idx, absmax
 
 
 # --------------------------------------------------------------------------

@@ -102,6 +102,45 @@ void oracle_dequant(const uint8_t *idx, const float *absmax, const float *codebo
 }
 
 /* ------------------------------------------------------------------------ */
+/* Quantisation ("load_in_4bit": the stored form the path starts from)        */
+/* ------------------------------------------------------------------------ */
+
+/* w [N,K] fp32 -> idx [N,K/2] (two codes per byte, even k in the low nibble)
+ * and absmax [N*K/block].  For each block of `block` consecutive elements of
+ * the row-major flattening: absmax = max |w| over the block; each element
+ * takes the code i that minimises |t - codebook[i]|, t = w / absmax computed
+ * as a double division (t = 0 when absmax is 0), each distance a double
+ * subtraction; the first (lowest) such i wins a tie.  The codebook need not
+ * be sorted.  Inputs are finite. */
+void oracle_quantize(const float *w, int64_t N, int64_t K, int64_t block, const float *codebook,
+                     uint8_t *idx, float *absmax)
+{
+    memset(idx, 0, (size_t)(N * K / 2));
+    for (int64_t b = 0; b < N * K / block; ++b) {
+        float a = 0.0f;
+        for (int64_t e = b * block; e < (b + 1) * block; ++e) {
+            float v = w[e] < 0.0f ? -w[e] : w[e];
+            if (v > a) a = v;
+        }
+        absmax[b] = a;
+        for (int64_t e = b * block; e < (b + 1) * block; ++e) {
+            double t = (a == 0.0f) ? 0.0 : (double)w[e] / (double)a;
+            unsigned best = 0;
+            double dbest = 0.0;
+            for (unsigned i = 0; i < 16; ++i) {
+                double d = t - (double)codebook[i];
+                if (d < 0.0) d = -d;
+                if (i == 0 || d < dbest) {
+                    best = i;
+                    dbest = d;
+                }
+            }
+            idx[e / 2] |= (uint8_t)((e % 2 == 0) ? best : (best << 4));
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Segment bookkeeping (several adapters side by side over N, e.g. fused QKV) */
 /* ------------------------------------------------------------------------ */
 
