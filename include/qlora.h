@@ -81,6 +81,22 @@ typedef struct {
  * block != 64), UNSUPPORTED (K % 64 != 0), ALIGNMENT, CUDA. */
 qlora_status dequant_4bit(const qlora_w4* w, void* out_bf16, float* out_f32, cudaStream_t stream);
 
+/* Quantise a weight W [N,K] to the storage above ("load_in_4bit"; pages:
+ * "Introducing Unsloth", section on QLoRA / load_in_4bit, and "利用 Unsloth
+ * 和 NVIDIA 硬件加速 LLM 训练", section 1).  W: device, row-major, fp32
+ * (w_is_bf16 == 0) or bf16 bit patterns (w_is_bf16 != 0); finite values.
+ * For each 64-block of the row-major flattening absmax = max |w|, and each
+ * element takes the first code i minimising |w/absmax - codebook[i]|, both
+ * the quotient and the differences in double precision (a zero block takes
+ * the code nearest 0).  The codebook (device, fp32 [16]) need not be sorted.
+ * Writes idx (device, uint8 [N, K/2], layout as in qlora_w4) and absmax
+ * (device, fp32 [N*K/64]).  The caller owns every buffer.
+ * Errors: INVALID_ARG (null pointer with N > 0, N < 0, K <= 0),
+ * UNSUPPORTED (K % 64 != 0), ALIGNMENT (W, idx or absmax not 16-byte
+ * aligned), CUDA. */
+qlora_status quantize_4bit(const void* W, int32_t w_is_bf16, int64_t N, int64_t K, const float* codebook,
+                           uint8_t* idx, float* absmax, cudaStream_t stream);
+
 /* Forward.  X bf16 [M,K]; A bf16 [K, n_seg*r]; B bf16 [r,N]; seg_n HOST int64
  * [n_seg] summing to N (may be NULL when n_seg == 1); s the LoRA scale.
  * Writes Y bf16 [M,N] and XA_save bf16 [M, n_seg*r] = bf16(X A) (pass it to

@@ -89,6 +89,8 @@ def lib(path: Optional[str] = None):
             L.qlora_launch_counter.argtypes = []
             L.qlora_debug_stall_next_launch.restype = None
             L.qlora_debug_stall_next_launch.argtypes = [ctypes.c_char_p]
+            L.quantize_4bit.restype = ctypes.c_int
+            L.quantize_4bit.argtypes = [P, I32, I64, I64, P, P, P, P]
             L.qlora_linear_xa_static.restype = ctypes.c_int
             L.qlora_linear_xa_static.argtypes = [P, I64, I64, P, I32, P, P]
             _lib = L
@@ -146,6 +148,11 @@ def _seg_array(seg_n: Optional[Sequence[int]]):
 
 def dequant_4bit(w: W4, out_bf16=None, out_f32=None, stream=None) -> None:
     _check(lib().dequant_4bit(ctypes.byref(w), _ptr(out_bf16), _ptr(out_f32), _stream(stream)), "dequant_4bit")
+
+
+def quantize_4bit(W, w_is_bf16: bool, N: int, K: int, codebook, idx, absmax, stream=None) -> None:
+    _check(lib().quantize_4bit(_ptr(W), 1 if w_is_bf16 else 0, int(N), int(K), _ptr(codebook), _ptr(idx),
+                               _ptr(absmax), _stream(stream)), "quantize_4bit")
 
 
 def qlora_linear_fwd(X, M: int, w: W4, A, B, r: int, seg_n, s: float, Y, XA_save, ws, ws_bytes: int,

@@ -80,6 +80,180 @@ __global__ void __launch_bounds__(256) dequant4_kernel(const uint32_t* __restric
   }
 }
 
+// 4-bit quantisation (the "load_in_4bit" storage the path starts from):
+// absmax = max |w| over each 64-block of the row-major flattening; the code
+// of an element is the first i minimising |t - codebook[i]|, t = w / absmax
+// as a double division (t = 0 for a zero block) and each distance a double
+// subtraction.  The codebook need not be sorted.
+//
+// The decision is made in fp32 first and confirmed in double only when fp32
+// cannot settle it (|t| <= 1 throughout):
+//  * sorted codebook: the code is the number of midpoints (c_i + c_{i+1})/2
+//    below t.  t32 = w * (1/absmax) (a correctly rounded division when
+//    absmax is tiny) is within 2^-22 of t and each fp32
+//    midpoint within 2^-24 max|c| of the exact one, so when t32 is farther
+//    than `margin` from both neighbouring midpoints, t lies strictly inside
+//    the same cell and the double argmin is that code, uniquely.
+//  * any codebook: a scan of the 16 fp32 distances (t32 = w / absmax,
+//    correctly rounded); every fp32 distance is within 2^-23 (1 + max|c|) of
+//    its double counterpart, so a best-vs-runner-up gap above `margin`
+//    settles the double argmin too.
+// Otherwise (ties, near ties -- rare) the 16 distances are recomputed in
+// double: exactly the definition.  In the sorted case a per-CTA table over
+// t settles almost every element with one shared-memory byte; elements in
+// the few buckets next to a midpoint take a branch-free binary search.  Eight lanes share a block: each converts
+// 8 consecutive weights (one 32-byte fp32 or 16-byte bf16 load), absmax is a
+// max over the 8 lanes, each lane writes its 4 packed bytes and the block's
+// first lane its absmax.
+__device__ __forceinline__ int quant_code_exact(float v, float am, const double* cb64) {
+  const double t = (am == 0.f) ? 0.0 : __ddiv_rn(static_cast<double>(v), static_cast<double>(am));
+  double db = 0.0;
+  int code = 0;
+  for (int i = 0; i < 16; ++i) {
+    const double d = fabs(__dsub_rn(t, cb64[i]));
+    if (i == 0 || d < db) {
+      db = d;
+      code = i;
+    }
+  }
+  return code;
+}
+
+constexpr int kQuantBuckets = 16384;  // table of the sorted-codebook quantiser (a multiple of 256)
+
+template <bool BF16_IN>
+__global__ void __launch_bounds__(256) quantize4_kernel(const void* __restrict__ w,
+                                                        const float* __restrict__ codebook, int64_t n_groups,
+                                                        uint32_t* __restrict__ idx4, float* __restrict__ absmax) {
+  __shared__ float cb[16];
+  __shared__ float mid[15];
+  __shared__ double cb64[16];
+  __shared__ int8_t lut[kQuantBuckets];
+  griddep_wait();
+  griddep_launch_dependents();
+  if (threadIdx.x < 16) {
+    cb[threadIdx.x] = codebook[threadIdx.x];
+    cb64[threadIdx.x] = static_cast<double>(codebook[threadIdx.x]);
+  }
+  __syncthreads();
+  if (threadIdx.x < 15) mid[threadIdx.x] = __fmul_rn(__fadd_rn(cb[threadIdx.x], cb[threadIdx.x + 1]), 0.5f);
+  __syncthreads();
+  float cmax = 0.f;
+  bool sorted = true;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    cmax = fmaxf(cmax, fabsf(cb[i]));
+    if (i > 0 && !(cb[i - 1] < cb[i])) sorted = false;
+  }
+  const float margin = 1.0e-6f * (1.0f + cmax);
+  const float mid7 = mid[7];
+  // Sorted codebook: bucket b of t covers [-1 + b*h, -1 + (b+1)*h), h =
+  // 2/kQuantBuckets.  The bucket index computed from t32 is within 1.2e-7 of
+  // exact, so when no midpoint lies within 2*margin of the bucket every t32
+  // that lands in it has the bucket's code with the margin to spare; the
+  // entry holds that code, else -1 (binary search instead).  Each thread
+  // fills a contiguous run of buckets, walking the sorted midpoints once.
+  {
+    const float h = 2.0f / static_cast<float>(kQuantBuckets);
+    const int per = kQuantBuckets / static_cast<int>(blockDim.x);
+    const int b0 = static_cast<int>(threadIdx.x) * per;
+    int pm = 0;
+    for (int b = b0; b < b0 + per; ++b) {
+      const float lo = -1.0f + static_cast<float>(b) * h;
+      const float hi = lo + h;
+      while (pm < 15 && mid[pm] < lo - 2.0f * margin) ++pm;
+      const bool clear = sorted && (pm == 15 || mid[pm] > hi + 2.0f * margin);
+      lut[b] = clear ? static_cast<int8_t>(pm) : static_cast<int8_t>(-1);
+    }
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const unsigned grp_mask = 0xFFu << (lane & 24);  // the 8 lanes of this block
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;  // a multiple of 8
+  // Software pipelined: the next group's load is issued before the current
+  // group is converted, so two loads per thread are in flight.
+  auto load8 = [&](int64_t g, float (&v)[8]) {
+    if (BF16_IN) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(w) + g);
+      const uint32_t q4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __uint_as_float(q4[j] << 16);
+        v[2 * j + 1] = __uint_as_float(q4[j] & 0xFFFF0000u);
+      }
+    } else {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(w) + 2 * g);
+      const float4 b = __ldg(reinterpret_cast<const float4*>(w) + 2 * g + 1);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+  };
+  int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  float nx[8];
+  if (g < n_groups) load8(g, nx);
+  for (; g < n_groups; g += stride) {
+    // n_groups is a multiple of 8 and the 8 lanes of a block start 8-aligned,
+    // so the 8 lanes of a block are all active here or all gone.
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = nx[j];
+    if (g + stride < n_groups) load8(g + stride, nx);
+    float am = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(v[j]));
+    am = fmaxf(am, __shfl_xor_sync(grp_mask, am, 1, 8));
+    am = fmaxf(am, __shfl_xor_sync(grp_mask, am, 2, 8));
+    am = fmaxf(am, __shfl_xor_sync(grp_mask, am, 4, 8));
+    uint32_t packed = 0;
+    if (sorted) {
+      // 1/absmax is a normal float only inside this range (it overflows
+      // below ~2.9e-39 and loses precision as a subnormal above ~8.5e37):
+      // divide outside it
+      const bool by_rcp = am >= 1.0e-37f && am <= 1.0e37f;
+      const float inv = by_rcp ? __frcp_rn(am) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float t32 = by_rcp ? __fmul_rn(v[j], inv) : (am == 0.f ? 0.f : __fdiv_rn(v[j], am));
+        const float xb = __fmaf_rn(t32, 0.5f * kQuantBuckets, 0.5f * kQuantBuckets);
+        int code = lut[min(max(static_cast<int>(xb), 0), kQuantBuckets - 1)];
+        if (code < 0) {
+          // number of midpoints below t32: branch-free binary search over the 15
+          code = (t32 > mid7) ? 8 : 0;
+          code += (t32 > mid[code + 3]) ? 4 : 0;
+          code += (t32 > mid[code + 1]) ? 2 : 0;
+          code += (t32 > mid[code]) ? 1 : 0;
+          const float lo = code > 0 ? fabsf(__fsub_rn(t32, mid[max(code - 1, 0)])) : INFINITY;
+          const float hi = code < 15 ? fabsf(__fsub_rn(mid[min(code, 14)], t32)) : INFINITY;
+          if (!(fminf(lo, hi) > margin)) code = quant_code_exact(v[j], am, cb64);
+        }
+        packed |= static_cast<uint32_t>(code) << (4 * j);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float t32 = (am == 0.f) ? 0.f : __fdiv_rn(v[j], am);
+        float d1 = INFINITY, d2 = INFINITY;
+        int code = 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float d = fabsf(__fsub_rn(t32, cb[i]));
+          if (d < d1) {
+            d2 = d1;
+            d1 = d;
+            code = i;
+          } else if (d < d2) {
+            d2 = d;
+          }
+        }
+        if (!(__fsub_rn(d2, d1) > margin)) code = quant_code_exact(v[j], am, cb64);
+        packed |= static_cast<uint32_t>(code) << (4 * j);
+      }
+    }
+    idx4[g] = packed;
+    if ((lane & 7) == 0) absmax[g >> 3] = am;
+  }
+}
+
 // Transposed dequantisation: outT[k,n] = deq(W)[n,k], outT is [K, N] with
 // row stride ldt elements.  One CTA converts a 64(n) x 64(k) tile through
 // shared memory so both the packed reads and the bf16 writes are coalesced.

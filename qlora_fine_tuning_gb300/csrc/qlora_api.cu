@@ -340,13 +340,23 @@ struct TileCfg {
   size_t smem;
 };
 
+// Ring depth cap of the rank-r GEMMs (QLORA_RED_STAGES overrides; 2..8).
+int red_stage_cap() {
+  static const int v = [] {
+    const char* e = std::getenv("QLORA_RED_STAGES");
+    const int n = e ? std::atoi(e) : kMaxStages;
+    return std::max(2, std::min(kMaxStages, n));
+  }();
+  return v;
+}
+
 // Ring geometry of gemm_tc_kernel; `red` reserves the split-sum buffer.
 TileCfg tile_cfg(int bn, bool red = false) {
   TileCfg c;
   c.bn = bn;
   c.stage_bytes = static_cast<uint32_t>(rup(kATileBytes + int64_t(bn) * 128, 1024));
   const int64_t ring = red ? int64_t(kSmemLimit) - kRedBytes - 1024 - 256 : 200 * 1024;
-  c.stages = std::min<int>(kMaxStages, static_cast<int>(ring / c.stage_bytes));
+  c.stages = std::min<int>(red ? red_stage_cap() : kMaxStages, static_cast<int>(ring / c.stage_bytes));
   c.smem = size_t(c.stages) * c.stage_bytes + (red ? kRedBytes : 0) + 1024 + 256;
   return c;
 }
@@ -421,7 +431,12 @@ int max_red_clusters(int splits, size_t smem) {
 // clusters of one wave fit on the device at once.
 template <bool A_MN, bool B_MN>
 int red_splits(int64_t tiles, int64_t nkb, size_t smem) {
-  const int64_t cap = std::min<int64_t>({int64_t(kMaxSplits), std::max<int64_t>(1, nkb),
+  static const int64_t most = [] {  // QLORA_RED_MAX_SPLITS caps the cluster size (1..8)
+    const char* e = std::getenv("QLORA_RED_MAX_SPLITS");
+    const int64_t n = e ? std::atoll(e) : kMaxSplits;
+    return std::max<int64_t>(1, std::min<int64_t>(kMaxSplits, n));
+  }();
+  const int64_t cap = std::min<int64_t>({most, std::max<int64_t>(1, nkb),
                                          std::max<int64_t>(1, int64_t(sm_count(cur_dev())) / std::max<int64_t>(tiles, 1))});
   for (int64_t sp = cap; sp > 1; --sp)
     if (max_red_clusters<A_MN, B_MN>(static_cast<int>(sp), smem) >= tiles) return static_cast<int>(sp);
@@ -723,6 +738,27 @@ qlora_status dequant_4bit(const qlora_w4* w, void* out_bf16, float* out_f32, cud
   if (!out_bf16 && !out_f32) return QLORA_ERR_INVALID_ARG;
   if ((out_bf16 && !al16(out_bf16)) || (out_f32 && !al16(out_f32))) return QLORA_ERR_ALIGNMENT;
   return launch_dequant(w, out_bf16, out_f32, st);
+}
+
+qlora_status quantize_4bit(const void* W, int32_t w_is_bf16, int64_t N, int64_t K, const float* codebook,
+                           uint8_t* idx, float* absmax, cudaStream_t st) {
+  if (N < 0 || K <= 0) return QLORA_ERR_INVALID_ARG;
+  if (K % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (N == 0) return QLORA_OK;
+  if (!W || !codebook || !idx || !absmax) return QLORA_ERR_INVALID_ARG;
+  if (!al16(W) || !al16(idx) || !al16(absmax)) return QLORA_ERR_ALIGNMENT;
+  const int64_t groups = N * K / 8;
+  // one wave (4 CTAs of 256 per SM): each CTA builds its table once
+  const int64_t blocks = std::min<int64_t>(cdiv(groups, 256), int64_t(kSMs) * 4);
+  LaunchScope ls("quantize4", st);
+  cudaError_t e;
+  if (w_is_bf16)
+    e = launch_k(quantize4_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, W, codebook, groups,
+                 reinterpret_cast<uint32_t*>(idx), absmax);
+  else
+    e = launch_k(quantize4_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, W, codebook, groups,
+                 reinterpret_cast<uint32_t*>(idx), absmax);
+  return cuda_status(e);
 }
 
 qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const void* A, const void* B, int32_t r,

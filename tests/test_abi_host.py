@@ -15,7 +15,7 @@ def L():
 
 def test_every_header_function_is_exported(L):
     names = b.header_functions()
-    assert {"dequant_4bit", "qlora_linear_fwd", "qlora_linear_bwd", "qlora_workspace_bytes",
+    assert {"dequant_4bit", "quantize_4bit", "qlora_linear_fwd", "qlora_linear_bwd", "qlora_workspace_bytes",
             "qlora_check_device_error", "qlora_status_str"} <= set(names)
     for n in names:
         assert hasattr(L, n), n
@@ -103,6 +103,18 @@ def test_dequant_argument_errors(L):
     assert L.dequant_4bit(ctypes.byref(w), FAKE, None, None) == b.UNSUPPORTED
     w = _w(N=0)
     assert L.dequant_4bit(ctypes.byref(w), FAKE, None, None) == b.OK  # nothing to do
+
+
+def test_quantize_argument_errors(L):
+    q = L.quantize_4bit
+    assert q(FAKE, 0, -1, 64, FAKE, FAKE, FAKE, None) == b.INVALID_ARG
+    assert q(FAKE, 0, 4, 0, FAKE, FAKE, FAKE, None) == b.INVALID_ARG
+    assert q(FAKE, 0, 4, 96, FAKE, FAKE, FAKE, None) == b.UNSUPPORTED
+    assert q(None, 0, 4, 64, FAKE, FAKE, FAKE, None) == b.INVALID_ARG
+    assert q(FAKE, 0, 4, 64, None, FAKE, FAKE, None) == b.INVALID_ARG
+    assert q(FAKE + 4, 0, 4, 64, FAKE, FAKE, FAKE, None) == b.ALIGNMENT
+    assert q(FAKE, 1, 4, 64, FAKE, FAKE + 8, FAKE, None) == b.ALIGNMENT
+    assert q(FAKE, 0, 0, 64, None, None, None, None) == b.OK  # nothing to do, nothing launched
 
 
 def test_profiler_collect_empty(L):
