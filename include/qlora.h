@@ -122,6 +122,17 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
                               const int64_t* seg_n, float s, void* dX, float* dA, float* dB, void* ws,
                               size_t ws_bytes, cudaStream_t stream);
 
+/* Backward for gradient accumulation over micro-batches: as qlora_linear_bwd
+ * (same arguments, same dX), but the adapter gradients are added into dA and
+ * dB instead of overwriting them: dA += s X^T G, dB += s XA^T dY, each element
+ * updated as fl32(old + fl32(s * sum)).  M == 0 leaves dA and dB unchanged.
+ * Page: "Introducing Unsloth", section 手动 Autograd (the adapter gradients);
+ * errors as for the forward. */
+qlora_status qlora_linear_bwd_accumulate(const void* dY, const void* X, const void* XA_saved, int64_t M,
+                                         const qlora_w4* W, const void* A, const void* B, int32_t r,
+                                         int32_t n_seg, const int64_t* seg_n, float s, void* dX, float* dA,
+                                         float* dB, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Workspace bytes needed by qlora_linear_fwd / qlora_linear_bwd for these
  * sizes (the larger of the two); 0 for invalid sizes. */
 size_t qlora_workspace_bytes(int64_t M, int64_t N, int64_t K, int32_t r, int32_t n_seg);

@@ -73,6 +73,8 @@ def lib(path: Optional[str] = None):
             L.qlora_linear_fwd.argtypes = [P, I64, WP, P, P, I32, I32, P, F, P, P, P, SZ, P]
             L.qlora_linear_bwd.restype = ctypes.c_int
             L.qlora_linear_bwd.argtypes = [P, P, P, I64, WP, P, P, I32, I32, P, F, P, P, P, P, SZ, P]
+            L.qlora_linear_bwd_accumulate.restype = ctypes.c_int
+            L.qlora_linear_bwd_accumulate.argtypes = [P, P, P, I64, WP, P, P, I32, I32, P, F, P, P, P, P, SZ, P]
             L.qlora_workspace_bytes.restype = SZ
             L.qlora_workspace_bytes.argtypes = [I64, I64, I64, I32, I32]
             L.qlora_check_device_error.restype = ctypes.c_int
@@ -171,6 +173,17 @@ def qlora_linear_bwd(dY, X, XA_saved, M: int, w: W4, A, B, r: int, seg_n, s: flo
                                 int(r), nseg, ctypes.cast(seg, ctypes.c_void_p) if seg is not None else None,
                                 float(s), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), int(ws_bytes), _stream(stream))
     _check(st, "qlora_linear_bwd")
+
+
+def qlora_linear_bwd_accumulate(dY, X, XA_saved, M: int, w: W4, A, B, r: int, seg_n, s: float, dX, dA, dB, ws,
+                                ws_bytes: int, stream=None) -> None:
+    seg, nseg = _seg_array(seg_n)
+    st = lib().qlora_linear_bwd_accumulate(_ptr(dY), _ptr(X), _ptr(XA_saved), int(M), ctypes.byref(w), _ptr(A),
+                                           _ptr(B), int(r), nseg,
+                                           ctypes.cast(seg, ctypes.c_void_p) if seg is not None else None,
+                                           float(s), _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws), int(ws_bytes),
+                                           _stream(stream))
+    _check(st, "qlora_linear_bwd_accumulate")
 
 
 def qlora_workspace_bytes(M: int, N: int, K: int, r: int, n_seg: int = 1) -> int:

@@ -104,7 +104,18 @@ struct GemmArgs {
   float* red_f32;             // red_scale * sum, row-major
   float* red_f32_t;           // red_scale * sum, transposed [col * red_ld_t + row]
   int64_t red_ld, red_ld_t;
+  int32_t red_accumulate;     // red_f32 / red_f32_t: add into the existing values instead of overwriting
 };
+
+// fp32 outputs of the split sum: v, or (accumulate) the existing value plus v.
+__device__ __forceinline__ float red_out1(const GemmArgs& p, const float* dst, float v) {
+  return p.red_accumulate ? __fadd_rn(*dst, v) : v;
+}
+__device__ __forceinline__ float4 red_out4(const GemmArgs& p, const float* dst, float4 v) {
+  if (!p.red_accumulate) return v;
+  const float4 o = *reinterpret_cast<const float4*>(dst);
+  return make_float4(__fadd_rn(o.x, v.x), __fadd_rn(o.y, v.y), __fadd_rn(o.z, v.z), __fadd_rn(o.w, v.w));
+}
 
 struct TileInfo {
   int m0, n0, split, red_begin, kb0, n_main, n_iter, b_row0, a2_x0, out_col0;
@@ -418,9 +429,10 @@ __global__ void __launch_bounds__(192, 1)
             // a warp's 32 rows are 32 consecutive outputs of each column
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              if (gcol + e < lim)
-                pq.red_f32_t[static_cast<int64_t>(gcol + e + t.out_col0) * pq.red_ld_t + grow] =
-                    __fmul_rn(pq.red_scale, __uint_as_float(v[e]));
+              if (gcol + e < lim) {
+                float* dst = pq.red_f32_t + static_cast<int64_t>(gcol + e + t.out_col0) * pq.red_ld_t + grow;
+                *dst = red_out1(pq, dst, __fmul_rn(pq.red_scale, __uint_as_float(v[e])));
+              }
           } else {
             const int64_t o = static_cast<int64_t>(grow) * pq.red_ld + t.out_col0 + gcol;
 #pragma unroll
@@ -441,10 +453,13 @@ __global__ void __launch_bounds__(192, 1)
               }
               if (pq.red_f32) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e)
-                  *reinterpret_cast<float4*>(pq.red_f32 + o + 8 * h + 4 * e) =
+                for (int e = 0; e < 2; ++e) {
+                  float* dst = pq.red_f32 + o + 8 * h + 4 * e;
+                  *reinterpret_cast<float4*>(dst) = red_out4(
+                      pq, dst,
                       make_float4(__fmul_rn(pq.red_scale, f[4 * e]), __fmul_rn(pq.red_scale, f[4 * e + 1]),
-                                  __fmul_rn(pq.red_scale, f[4 * e + 2]), __fmul_rn(pq.red_scale, f[4 * e + 3]));
+                                  __fmul_rn(pq.red_scale, f[4 * e + 2]), __fmul_rn(pq.red_scale, f[4 * e + 3])));
+                }
               }
             }
           }
@@ -530,9 +545,10 @@ __global__ void __launch_bounds__(192, 1)
             const float f[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
             if (tr) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                pq.red_f32_t[static_cast<int64_t>(gcol + e + t.out_col0) * pq.red_ld_t + grow] =
-                    __fmul_rn(pq.red_scale, f[e]);
+              for (int e = 0; e < 4; ++e) {
+                float* dst = pq.red_f32_t + static_cast<int64_t>(gcol + e + t.out_col0) * pq.red_ld_t + grow;
+                *dst = red_out1(pq, dst, __fmul_rn(pq.red_scale, f[e]));
+              }
               continue;
             }
             const int64_t o = static_cast<int64_t>(grow) * pq.red_ld + t.out_col0 + gcol;
@@ -544,8 +560,9 @@ __global__ void __launch_bounds__(192, 1)
                              pack_bf16x2(__fmul_rn(pq.red_scale, f[2]), __fmul_rn(pq.red_scale, f[3])));
             if (pq.red_f32)
               *reinterpret_cast<float4*>(pq.red_f32 + o) =
-                  make_float4(__fmul_rn(pq.red_scale, f[0]), __fmul_rn(pq.red_scale, f[1]),
-                              __fmul_rn(pq.red_scale, f[2]), __fmul_rn(pq.red_scale, f[3]));
+                  red_out4(pq, pq.red_f32 + o,
+                           make_float4(__fmul_rn(pq.red_scale, f[0]), __fmul_rn(pq.red_scale, f[1]),
+                                       __fmul_rn(pq.red_scale, f[2]), __fmul_rn(pq.red_scale, f[3])));
           }
         }
         // 6. done reading this round: arrive (release) on every CTA's red_free

@@ -863,9 +863,13 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
   return QLORA_OK;
 }
 
-qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_saved, int64_t M, const qlora_w4* W,
-                              const void* A, const void* B, int32_t r, int32_t n_seg, const int64_t* seg_n, float s,
-                              void* dX, float* dA, float* dB, void* ws, size_t ws_bytes, cudaStream_t st) {
+}  // extern "C"
+
+namespace {
+// Backward; `accumulate` adds the adapter gradients into dA and dB.
+qlora_status linear_bwd(const void* dY, const void* X, const void* XA_saved, int64_t M, const qlora_w4* W,
+                        const void* A, const void* B, int32_t r, int32_t n_seg, const int64_t* seg_n, float s,
+                        void* dX, float* dA, float* dB, void* ws, size_t ws_bytes, cudaStream_t st, bool accumulate) {
   Segs sg;
   QL_TRY(check_layer(M, W, r, n_seg, seg_n, &sg));
   if (!dY || !X || !XA_saved || !A || !B || !dA || !dB) return QLORA_ERR_INVALID_ARG;
@@ -879,6 +883,7 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
   if (ws_bytes < L.total) return QLORA_ERR_WORKSPACE;
   const int64_t R = L.R;
   if (M == 0) {
+    if (accumulate) return QLORA_OK;  // nothing to add
     QL_TRY(cuda_status(cudaMemsetAsync(dA, 0, size_t(K) * R * 4, st)));
     QL_TRY(cuda_status(cudaMemsetAsync(dB, 0, size_t(r) * N * 4, st)));
     return QLORA_OK;
@@ -993,6 +998,7 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     ga.red_scale = s;
     ga.red_f32 = dA;
     ga.red_ld = R;
+    ga.red_accumulate = accumulate ? 1 : 0;
     GemmArgs gb = base_args(err);
     gb.M = static_cast<int32_t>(N);
     gb.N = r;
@@ -1005,11 +1011,28 @@ qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_save
     gb.red_scale = s;
     gb.red_f32_t = dB;
     gb.red_ld_t = N;
+    gb.red_accumulate = accumulate ? 1 : 0;
     const RedProb pb{gb, mdYmn, mXAmn, nt, 1, 1, bn_b};
     QL_TRY((launch_gemm_red<true, true>("gemm_dadb", splits, tc, RedProb{ga, mXmn, mGmn, kt, 1, 1, bn_a}, &pb,
                                         st)));
   }
   return QLORA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+qlora_status qlora_linear_bwd(const void* dY, const void* X, const void* XA_saved, int64_t M, const qlora_w4* W,
+                              const void* A, const void* B, int32_t r, int32_t n_seg, const int64_t* seg_n, float s,
+                              void* dX, float* dA, float* dB, void* ws, size_t ws_bytes, cudaStream_t st) {
+  return linear_bwd(dY, X, XA_saved, M, W, A, B, r, n_seg, seg_n, s, dX, dA, dB, ws, ws_bytes, st, false);
+}
+
+qlora_status qlora_linear_bwd_accumulate(const void* dY, const void* X, const void* XA_saved, int64_t M,
+                                         const qlora_w4* W, const void* A, const void* B, int32_t r, int32_t n_seg,
+                                         const int64_t* seg_n, float s, void* dX, float* dA, float* dB, void* ws,
+                                         size_t ws_bytes, cudaStream_t st) {
+  return linear_bwd(dY, X, XA_saved, M, W, A, B, r, n_seg, seg_n, s, dX, dA, dB, ws, ws_bytes, st, true);
 }
 
 }  // extern "C"

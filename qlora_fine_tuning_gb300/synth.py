@@ -198,6 +198,11 @@ WORKLOADS = {
         ("up", dict(M=8192, K=4096, N=14336, r=64, s=0.25)),
         ("down", dict(M=8192, K=14336, N=4096, r=64, s=0.25)),
     ],
+    # gate and up as one call: W_gate and W_up stacked, one adapter per half
+    "llama3-8b-mlp-fused-gateup-m8192-4096x2x14336-r64": [
+        ("gate_up", dict(M=8192, K=4096, N=28672, r=64, s=0.25, seg_n=(14336, 14336))),
+        ("down", dict(M=8192, K=14336, N=4096, r=64, s=0.25)),
+    ],
     "qwen3-14b-mlp-m16384-5120x17408-r16": [
         ("gate", dict(M=16384, K=5120, N=17408, r=16, s=2.0, with_lengths=True)),
         ("up", dict(M=16384, K=5120, N=17408, r=16, s=2.0, with_lengths=True)),

@@ -214,6 +214,7 @@ FULL = [
     ("llama3-8b-mlp-m8192-4096x14336-r64", 0),   # gate
     ("llama3-8b-mlp-m8192-4096x14336-r64", 2),   # down
     ("qwen3-14b-mlp-m16384-5120x17408-r16", 0),  # gate
+    ("llama3-8b-mlp-fused-gateup-m8192-4096x2x14336-r64", 0),  # gate and up as one two-adapter call
 ]
 
 
