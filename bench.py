@@ -166,6 +166,45 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+PAIR_PROFILE = os.path.join(ROOT, "profiles", "gemm_pair_llama3-8b-mlp.md")
+DEFAULT_WORKLOAD = "llama3-8b-mlp-m8192-4096x14336-r64"
+
+
+def pair_sources_sha256() -> str:
+    """sha256 of what decides the pair GEMM's DRAM traffic: its kernel source,
+    the PTX wrappers and the host's tile-order choice (pair_group())."""
+    import hashlib
+    import re
+    csrc = os.path.join(ROOT, "qlora_fine_tuning_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm_pair.cuh", "ptx.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    with open(os.path.join(csrc, "qlora_api.cu")) as fh:
+        m = re.search(r"int pair_group\(.*?\n}\n", fh.read(), re.S)
+    h.update(m.group(0).encode() if m else b"")
+    return h.hexdigest()
+
+
+def pair_traffic(workload: str):
+    """(bytes per launch, note): the ncu DRAM bytes committed under profiles/
+    for this workload's pair-GEMM launches, while the sources still match the
+    capture; else (None, why)."""
+    if workload != DEFAULT_WORKLOAD:
+        return None, "captured for the Llama-3-8B MLP workload only"
+    try:
+        with open(PAIR_PROFILE) as fh:
+            text = fh.read()
+        val = int(text.split("traffic_bytes_per_launch:")[1].split()[0])
+        sha = text.split("sources_sha256:")[1].split()[0]
+    except (OSError, IndexError, ValueError):
+        return None, "no capture under profiles/"
+    if sha != pair_sources_sha256():
+        return None, "kernel or tile order changed since the ncu capture under profiles/"
+    return val, ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, averaged over the step's "
+                 "six pair-GEMM launches; profiles/gemm_pair_llama3-8b-mlp.md")
+
+
 def run_ours(args, rank, world):
     import torch
     from qlora_fine_tuning_gb300 import binding
@@ -288,17 +327,20 @@ def run_ours(args, rank, world):
     main_launches = sum(ktimes.get(k, (0, 0.0))[0] for k in ("gemm_fwd", "gemm_dx"))
     achieved = main_flops_step * prof_steps / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    traffic, traffic_note = pair_traffic(args.workload)
+    # A, B (dequantised weight) and C once per launch, averaged over the step's launches
+    alg_bytes = sum(2 * (li.M * li.K + li.N * li.K + li.M * li.N) * 2 for li in lins) / (2 * len(lins))
     roofline = {
-        "kernel": "gemm_tc_kernel (forward Y and backward dX instances)",
+        "kernel": "gemm_pair_kernel (forward Y and backward dX instances)",
         "bound": "tensor",
         "achieved": round(achieved, 2) if achieved else None,
         "peak": peak,
         "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
         "unit": "TFLOP/s",
         "frac": round(achieved / peak, 4) if achieved else None,
-        "traffic": None,
-        "traffic_note": "per-launch DRAM bytes differ by linear; the ncu capture of the gate forward launch "
-                        "(read 1.083 GB + write 0.222 GB vs 0.422 GB algorithmic) is in profiles/",
+        "traffic": traffic,
+        "traffic_note": traffic_note,
+        "algorithmic_bytes_per_launch": int(alg_bytes),
         "launches": main_launches,
         "avg_launch_ms": round(main_ms / max(1, main_launches), 4),
         "timing": f"CUDA events around each launch on the launching stream, {prof_steps} steps run "

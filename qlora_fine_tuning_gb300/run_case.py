@@ -5,7 +5,9 @@ A small driver for profilers (ncu) and for quick timing of a single call:
     python -m qlora_fine_tuning_gb300.run_case --workload llama3-8b-mlp-m8192-4096x14336-r64 \
         --linear 0 --rows 4096 --op fwd --iters 3
 
---rows overrides M (the number of tokens) to keep a capture small.
+--rows overrides M (the number of tokens) to keep a capture small.  --op quantize
+quantises a seeded fp32 weight of the linear's shape (into the linear's
+code and absmax buffers).
 Prints the per-iteration CUDA-event time of the requested call.
 """
 from __future__ import annotations
@@ -20,7 +22,7 @@ def main():
     p.add_argument("--workload", default="llama3-8b-mlp-m8192-4096x14336-r64")
     p.add_argument("--linear", type=int, default=0)
     p.add_argument("--rows", type=int, default=0)
-    p.add_argument("--op", default="fwd", choices=["fwd", "bwd", "both", "dequant"])
+    p.add_argument("--op", default="fwd", choices=["fwd", "bwd", "both", "dequant", "quantize"])
     p.add_argument("--iters", type=int, default=3)
     a = p.parse_args()
 
@@ -48,8 +50,15 @@ def main():
     Wd = torch.empty((li.N, li.K), dtype=torch.bfloat16, device="cuda")
     ws, ws_bytes = binding.alloc_workspace(li.M, li.N, li.K, li.r, len(li.seg_n))
     seg = None if len(li.seg_n) == 1 else list(li.seg_n)
+    if a.op == "quantize":  # a seeded fp32 weight of the linear's shape, quantised on the GPU
+        gq = torch.Generator(device="cuda")
+        gq.manual_seed(0)
+        Wf = torch.randn((li.N, li.K), generator=gq, device="cuda", dtype=torch.float32) * 0.02
 
     def call():
+        if a.op == "quantize":
+            binding.quantize_4bit(Wf, False, li.N, li.K, cb, idx, absmax)
+            return
         if a.op == "dequant":
             binding.dequant_4bit(w, Wd)
             return
