@@ -75,7 +75,8 @@ def test_accumulate_onto_zeros_equals_overwrite_and_empty_batch_is_a_no_op():
 
 def test_fused_gate_up_forward_equals_two_separate_calls():
     """One two-adapter call over N = 2 x 14336 against the gate and up calls
-    made separately: the forward outputs are the same numbers, bit for bit."""
+    made separately: XA and Y are the same numbers, bit for bit (every tile
+    sums the same products in the same order)."""
     import torch
     label, kw = synth.WORKLOADS["llama3-8b-mlp-fused-gateup-m8192-4096x2x14336-r64"][0]
     li = synth.make_linear(seed=0, stream=0, **kw)

@@ -108,6 +108,9 @@ SMALL = [
     (200, 320, 128, 16, 1.0, (128, 128, 64)), # three adapters side by side
     (64, 384, 192, 8, 2.0, (256, 128)),       # rank 8 with two adapters
     (2048, 2560, 512, 16, 1.0, None),         # more tiles than CTA pairs; rank-r rounds between tiles
+    # 81 pair tiles: one full wave of 76 pairs and a 5-tile tail
+    (2304, 2304, 1024, 64, 0.25, (1280, 1024)),  # ... in the forward GEMM (two adapters)
+    (2304, 1024, 2304, 16, 1.0, None),           # ... in the dX GEMM
 ]
 
 
@@ -170,8 +173,9 @@ def test_empty_batch():
     assert float(g.dA.abs().max()) == 0.0 and float(g.dB.abs().max()) == 0.0
 
 
-def test_deterministic_repeat():
-    li = synth.make_linear(300, 384, 256, 16, 1.0, seed=21)
+@pytest.mark.parametrize("M,N,K", [(300, 384, 256), (2304, 2304, 2304)])
+def test_deterministic_repeat(M, N, K):
+    li = synth.make_linear(M, N, K, 16, 1.0, seed=21)
     g = GpuLayer(li)
     g.forward()
     g.backward()
