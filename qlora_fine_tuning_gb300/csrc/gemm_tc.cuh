@@ -67,7 +67,7 @@ enum GemmEpi : int {
 constexpr int kMaxSeg = 8;
 constexpr uint32_t kRedLd = 68;                     // floats per row of the reduction buffer (64 + 4 pad)
 constexpr uint32_t kRedBytes = 128u * kRedLd * 4u;  // one 128 x 64 fp32 chunk
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 10;
 constexpr uint32_t kATileBytes = 128 * 128;  // 128 rows x 64 bf16
 
 struct GemmArgs {
@@ -105,6 +105,7 @@ struct GemmArgs {
   float* red_f32_t;           // red_scale * sum, transposed [col * red_ld_t + row]
   int64_t red_ld, red_ld_t;
   int32_t red_accumulate;     // red_f32 / red_f32_t: add into the existing values instead of overwriting
+  int32_t red_in_ring;        // every cluster has one tile: the split-sum buffer reuses ring stage 0
 };
 
 // fp32 outputs of the split sum: v, or (accumulate) the existing value plus v.
@@ -199,8 +200,12 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((((raw + 1023u) & ~1023u)) - raw);
-  float* red = reinterpret_cast<float*>(smem + static_cast<uint32_t>(p.stages) * p.stage_bytes);
-  uint8_t* ctrl = reinterpret_cast<uint8_t*>(red) + (RED ? kRedBytes : 0u);
+  // The split-sum buffer follows the ring, or -- when each cluster takes one
+  // tile, so that the ring is idle once that tile's MMAs have completed --
+  // occupies the start of the ring itself.
+  const bool in_ring = RED && p.red_in_ring;
+  float* red = reinterpret_cast<float*>(in_ring ? smem : smem + static_cast<uint32_t>(p.stages) * p.stage_bytes);
+  uint8_t* ctrl = smem + static_cast<uint32_t>(p.stages) * p.stage_bytes + ((RED && !in_ring) ? kRedBytes : 0u);
   uint64_t* full = reinterpret_cast<uint64_t*>(ctrl);
   uint64_t* empty = full + kMaxStages;
   uint64_t* tfull = empty + kMaxStages;   // [2] accumulator ready

@@ -340,7 +340,17 @@ struct TileCfg {
   size_t smem;
 };
 
-// Ring depth cap of the rank-r GEMMs (QLORA_RED_STAGES overrides; 2..8).
+// Split-sum buffer inside the idle ring when each cluster has one tile
+// (QLORA_RED_IN_RING=0 turns it off).
+bool red_in_ring_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("QLORA_RED_IN_RING");
+    return !(e && e[0] == '0');
+  }();
+  return on;
+}
+
+// Ring depth cap of the rank-r GEMMs (QLORA_RED_STAGES overrides; 2..10).
 int red_stage_cap() {
   static const int v = [] {
     const char* e = std::getenv("QLORA_RED_STAGES");
@@ -350,14 +360,17 @@ int red_stage_cap() {
   return v;
 }
 
-// Ring geometry of gemm_tc_kernel; `red` reserves the split-sum buffer.
-TileCfg tile_cfg(int bn, bool red = false) {
+// Ring geometry of gemm_tc_kernel; `red` reserves the split-sum buffer after
+// the ring, `in_ring` puts it inside the ring instead (one tile per cluster).
+TileCfg tile_cfg(int bn, bool red = false, bool in_ring = false) {
   TileCfg c;
   c.bn = bn;
   c.stage_bytes = static_cast<uint32_t>(rup(kATileBytes + int64_t(bn) * 128, 1024));
-  const int64_t ring = red ? int64_t(kSmemLimit) - kRedBytes - 1024 - 256 : 200 * 1024;
-  c.stages = std::min<int>(red ? red_stage_cap() : kMaxStages, static_cast<int>(ring / c.stage_bytes));
-  c.smem = size_t(c.stages) * c.stage_bytes + (red ? kRedBytes : 0) + 1024 + 256;
+  const int64_t extra = (red && !in_ring) ? kRedBytes : 0;
+  const int64_t ring = red ? int64_t(kSmemLimit) - extra - 1024 - 256 : 200 * 1024;
+  c.stages = std::min<int>(red ? red_stage_cap() : 8, static_cast<int>(ring / c.stage_bytes));
+  if (in_ring && int64_t(c.stages) * c.stage_bytes < int64_t(kRedBytes)) c.stages = 0;  // caller falls back
+  c.smem = size_t(c.stages) * c.stage_bytes + extra + 1024 + 256;
   return c;
 }
 
@@ -455,7 +468,7 @@ struct RedProb {
 // gemm_tc_kernel<.., EPI_RED>: `splits` CTAs per tile in one cluster; an
 // optional second problem shares the launch (its tiles follow the first's).
 template <bool A_MN, bool B_MN>
-qlora_status launch_gemm_red(const char* name, int splits, const TileCfg& tc, RedProb p1, const RedProb* p2,
+qlora_status launch_gemm_red(const char* name, int splits, const TileCfg& tc_in, RedProb p1, const RedProb* p2,
                              cudaStream_t st) {
   auto kern = gemm_tc_kernel<A_MN, B_MN, EPI_RED>;
   static std::once_flag attr_once[64];
@@ -464,6 +477,13 @@ qlora_status launch_gemm_red(const char* name, int splits, const TileCfg& tc, Re
   std::call_once(attr_once[dev & 63], [kern] {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   });
+  const int64_t tiles = p1.m_tiles * p1.n_tiles * p1.zseg + (p2 ? p2->m_tiles * p2->n_tiles * p2->zseg : 0);
+  const int64_t clusters = std::min<int64_t>(tiles, max_red_clusters<A_MN, B_MN>(splits, tc_in.smem));
+  // One tile per cluster: the split-sum buffer can share the ring, which then
+  // gets the 34 KB the buffer would occupy (QLORA_RED_IN_RING=0 keeps them apart).
+  const TileCfg ring_tc = tile_cfg(tc_in.bn, true, true);
+  const bool in_ring = tiles <= clusters && ring_tc.stages > tc_in.stages && red_in_ring_enabled();
+  const TileCfg& tc = in_ring ? ring_tc : tc_in;
   auto fill = [&](RedProb& pr) {
     GemmArgs& a = pr.g;
     a.bn = pr.bn;
@@ -472,6 +492,7 @@ qlora_status launch_gemm_red(const char* name, int splits, const TileCfg& tc, Re
     a.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     a.l2_hints = 0;
     a.splits = splits;
+    a.red_in_ring = in_ring ? 1 : 0;
     a.m_tiles = static_cast<int32_t>(pr.m_tiles);
     a.n_tiles = static_cast<int32_t>(pr.n_tiles);
     a.z_tiles = static_cast<int32_t>(pr.zseg * splits);
@@ -487,8 +508,6 @@ qlora_status launch_gemm_red(const char* name, int splits, const TileCfg& tc, Re
     q2.a = p1.a;
     q2.b = p1.b;
   }
-  const int64_t tiles = p1.m_tiles * p1.n_tiles * p1.zseg + (p2 ? p2->m_tiles * p2->n_tiles * p2->zseg : 0);
-  const int64_t clusters = std::min<int64_t>(tiles, max_red_clusters<A_MN, B_MN>(splits, tc.smem));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * splits));
   cfg.blockDim = dim3(192);
