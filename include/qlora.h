@@ -81,9 +81,9 @@ typedef struct {
  * block != 64), UNSUPPORTED (K % 64 != 0), ALIGNMENT, CUDA. */
 qlora_status dequant_4bit(const qlora_w4* w, void* out_bf16, float* out_f32, cudaStream_t stream);
 
-/* Quantise a weight W [N,K] to the storage above ("load_in_4bit"; pages:
- * "Introducing Unsloth", section on QLoRA / load_in_4bit, and "利用 Unsloth
- * 和 NVIDIA 硬件加速 LLM 训练", section 1).  W: device, row-major, fp32
+/* Quantise a weight W [N,K] to the storage above (the models are loaded with
+ * load_in_4bit=True: page "利用 Unsloth 和 NVIDIA 硬件加速 LLM 训练", section
+ * 代码实战, and its section 1 on 4-bit weights).  W: device, row-major, fp32
  * (w_is_bf16 == 0) or bf16 bit patterns (w_is_bf16 != 0); finite values.
  * For each 64-block of the row-major flattening absmax = max |w|, and each
  * element takes the first code i minimising |w/absmax - codebook[i]|, both

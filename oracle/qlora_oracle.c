@@ -102,7 +102,9 @@ void oracle_dequant(const uint8_t *idx, const float *absmax, const float *codebo
 }
 
 /* ------------------------------------------------------------------------ */
-/* Quantisation ("load_in_4bit": the stored form the path starts from)        */
+/* Quantisation: the stored form the path starts from (the pages load the    */
+/* model with load_in_4bit=True -- "利用 Unsloth 和 NVIDIA 硬件加速 LLM 训练",  */
+/* section 代码实战; the 4-bit format itself is the reading in the header)    */
 /* ------------------------------------------------------------------------ */
 
 /* w [N,K] fp32 -> idx [N,K/2] (two codes per byte, even k in the low nibble)

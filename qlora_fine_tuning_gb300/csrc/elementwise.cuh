@@ -80,7 +80,9 @@ __global__ void __launch_bounds__(256) dequant4_kernel(const uint32_t* __restric
   }
 }
 
-// 4-bit quantisation (the "load_in_4bit" storage the path starts from):
+// 4-bit quantisation (the storage the path starts from; the pages load their
+// models with load_in_4bit=True -- "利用 Unsloth 和 NVIDIA 硬件加速 LLM 训练",
+// section 代码实战):
 // absmax = max |w| over each 64-block of the row-major flattening; the code
 // of an element is the first i minimising |t - codebook[i]|, t = w / absmax
 // as a double division (t = 0 for a zero block) and each distance a double
