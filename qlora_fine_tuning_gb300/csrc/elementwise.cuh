@@ -1,7 +1,8 @@
 // elementwise.cuh -- HBM-bound kernels of the QLoRA linear path:
 //   * 4-bit -> bf16 (and fp32) dequantisation, row-major and transposed
-//   * small transposes of the rank-r operands
-//   * deterministic reductions of split partial sums
+//   * 4-bit quantisation of a fp32 / bf16 weight (the stored form)
+//   * small transposes and deterministic reductions of split partial sums,
+//     used by the single-CTA fallback and the static-scratch XA entry point
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>

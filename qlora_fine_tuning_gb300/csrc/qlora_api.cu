@@ -1,18 +1,23 @@
 // qlora_api.cu -- host side of libqlora.so: argument checks, workspace
 // carving, TMA descriptor encoding, launch sequencing, profiler.
 //
-// Forward (one call):
+// Forward (one call, 3 launches):
 //   dequant W -> Wd bf16 [N,K]            (elementwise, HBM-bound)
-//   A -> A^T [R,K], B -> B^T [N,Rp]       (tiny transposes; Rp = r rounded to 16)
-//   XA = X . A        tcgen05, split over K, fp32 partials -> XA_save, s*XA (bf16)
-//   Y  = X . Wd^T + (s*XA) . B   tcgen05, the rank-r product as extra K-steps
-//                                 into the same TMEM accumulator
-// Backward (one call):
-//   G  = dY . B^T per segment     tcgen05, split over N -> s*G [M,R], G^T [R,M]
-//   dequant W transposed -> Wd^T bf16 [K,N]
-//   dX = dY . Wd + (s*G) . A^T    tcgen05, rank-r product as extra K-steps
-//   dA = s X^T G      tcgen05 with X read MN-major, split over M
-//   dB = s XA^T dY    tcgen05 with dY read MN-major, split over M
+//   XA = X . A        rank-r GEMM, A read MN-major as stored; the splits of K
+//                     are summed on chip -> XA_save and s*XA (bf16)
+//   Y  = X . Wd^T + (s*XA) . B   CTA-pair GEMM, the rank-r product as extra
+//                                 K-steps into the same TMEM accumulator
+//                                 (B read MN-major as stored)
+// Backward (one call, 4 launches):
+//   G  = dY . B^T per segment     rank-r GEMM, splits of N summed on chip
+//                                 -> s*G and G [M,R]
+//   dequant W -> Wd bf16 [N,K]    (read MN-major by the dX GEMM)
+//   dX = dY . Wd + (s*G) . A^T    CTA-pair GEMM, rank-r product as extra K-steps
+//   dA = s X^T G and dB = s XA^T dY   one rank-r launch with two problems,
+//                                 every operand read MN-major as stored
+// When adapter boundaries are not multiples of 256 columns (or pairs are
+// disabled) the products run on the single-CTA GEMM instead, with B^T and the
+// transposed dequantisation it needs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -589,8 +594,6 @@ qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles
   return cuda_status(e);
 }
 
-// Let the kernel finish its split reduction when there are counters for all
-// of its output tiles; otherwise the caller runs reduce_tile_kernel.
 GemmArgs base_args(uint32_t* err) {
   GemmArgs g;
   std::memset(&g, 0, sizeof(g));
