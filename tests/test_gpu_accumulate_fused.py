@@ -73,6 +73,23 @@ def test_accumulate_onto_zeros_equals_overwrite_and_empty_batch_is_a_no_op():
     assert np.array_equal(again["dA"], ref["dA"]) and np.array_equal(again["dB"], ref["dB"])
 
 
+def test_accumulate_without_dx_leaves_dx_untouched():
+    import torch
+    li = synth.make_linear(192, 256, 128, 8, 2.0, seed=47)
+    g = GpuLayer(li)
+    g.forward()
+    g.dX.fill_(3.0)
+    g.dA.zero_()
+    g.dB.zero_()
+    binding.qlora_linear_bwd_accumulate(g.dY, g.X, g.XA, li.M, g.w, g.A, g.B, li.r, None, li.s, None, g.dA, g.dB,
+                                        g.ws, g.ws_bytes)
+    g.check()
+    got = g.results()
+    assert np.all(got["dX"] == 3.0)
+    ref = oracle_full(li)
+    compare(got, ref, keys=("dA", "dB"))
+
+
 def test_fused_gate_up_forward_equals_two_separate_calls():
     """One two-adapter call over N = 2 x 14336 against the gate and up calls
     made separately: XA and Y are the same numbers, bit for bit (every tile
