@@ -73,6 +73,38 @@ def test_accumulate_onto_zeros_equals_overwrite_and_empty_batch_is_a_no_op():
     assert np.array_equal(again["dA"], ref["dA"]) and np.array_equal(again["dB"], ref["dB"])
 
 
+def test_row_shards_accumulate_to_the_full_batch():
+    """Data-parallel stand-in on one GPU: the backward of the first half of the
+    rows, then the second half accumulated into the same dA, dB, equals the
+    full batch's gradients (to 2e-3: the halves pick other split counts, so G can
+    round differently in bf16)."""
+    import torch
+    li = synth.make_linear(640, 512, 384, 16, 0.5, seed=53)
+    full = GpuLayer(li)
+    full.forward()
+    full.backward()
+    full.check()
+    ref = full.results()
+    h = 320
+    parts = []
+    for rows in (slice(0, h), slice(h, li.M)):
+        parts.append(synth.LinearInputs(M=h, N=li.N, K=li.K, r=li.r, s=li.s, seg_n=li.seg_n, idx=li.idx,
+                                        absmax=li.absmax, codebook=li.codebook, X=li.X[rows], A=li.A, B=li.B,
+                                        dY=li.dY[rows]))
+    g = GpuLayer(parts[0])
+    g.forward()
+    g.backward()
+    g2 = GpuLayer(parts[1])
+    g2.forward()
+    binding.qlora_linear_bwd_accumulate(g2.dY, g2.X, g2.XA, h, g2.w, g2.A, g2.B, li.r, None, li.s, g2.dX, g.dA, g.dB,
+                                        g2.ws, g2.ws_bytes)
+    g2.check()
+    got = g.results()
+    compare({"dA": got["dA"], "dB": got["dB"]}, {"dA": ref["dA"], "dB": ref["dB"]}, keys=("dA", "dB"), tol=2e-3)
+    # and against the oracle's full batch
+    compare({"dA": got["dA"], "dB": got["dB"]}, oracle_full(li), keys=("dA", "dB"))
+
+
 def test_accumulate_without_dx_leaves_dx_untouched():
     import torch
     li = synth.make_linear(192, 256, 128, 8, 2.0, seed=47)
