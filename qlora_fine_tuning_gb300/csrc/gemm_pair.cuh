@@ -178,8 +178,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 448 : 192
     const uint32_t tx_pair = 2u * kPairStageBytes;
     const uint32_t tx_a_pair = 2u * kATileBytes;
     const uint32_t tx_raw = B_MN ? 4096u + 1024u : 4096u + 2048u;
-    const uint64_t pol_a = (p.l2_hints & 2) ? l2_policy_evict_last() : l2_policy_evict_normal();
-    const uint64_t pol_b = (p.l2_hints & 4) ? l2_policy_evict_first() : l2_policy_evict_normal();
+    // The operand of the current band is re-read by the band's tiles: keep it
+    // (evict-last); the other operand streams past once per band (evict-first).
+    // Row bands hold rows of A, column bands (group_m < 0) columns of B.
+    const bool band_is_b = p.group_m < 0 && -p.group_m < p.n_tiles;
+    const uint64_t keep = (p.l2_hints & 2) ? l2_policy_evict_last() : l2_policy_evict_normal();
+    const uint64_t pass = (p.l2_hints & 4) ? l2_policy_evict_first() : l2_policy_evict_normal();
+    const uint64_t pol_a = band_is_b ? pass : keep;
+    const uint64_t pol_b = band_is_b ? keep : pass;
     uint32_t g = 0;
     uint32_t raw_issued = 0;  // bit i: ring position g-1-i had a packed-code load in flight
     bool ok = true;

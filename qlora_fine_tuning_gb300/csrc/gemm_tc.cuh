@@ -93,7 +93,7 @@ struct GemmArgs {
   uint64_t timeout_ns;  // bound on every barrier wait
   int32_t debug_stall;  // test hook: CTA (pair) 0 never fills its first stage
   int32_t l2_hints;     // bit 0: streaming (evict-first) output stores;
-                        // bit 1: A loads evict-last; bit 2: B loads evict-first
+                        // bit 1: the band's operand evict-last; bit 2: the other evict-first
   int32_t group_m;        // pair kernel tile order: >0 row tiles per band, <0 column tiles per band, 0 one band
   const float* codebook;  // 16 fp32 values (pair kernel with in-kernel dequantisation)
   int32_t dq_k;           // K of the 4-bit weight (pair kernel with in-kernel dequantisation)
