@@ -389,7 +389,7 @@ __device__ __forceinline__ void tc_mma_bf16_pair_k64_ws(uint32_t d_tmem, uint64_
       : "memory");
 }
 
-// Out-of-line bounded wait for a whole warp: lane 0 polls, the outcome is
+// Out-of-line bounded wait for a whole warp: lane 0 polls, the verdict is
 // broadcast.  Kept out of line so the issue loops that call it only on a
 // miss stay short (a bounded wait loop inlined into an MMA issue loop was
 // measured to halve the MMA issue rate).
