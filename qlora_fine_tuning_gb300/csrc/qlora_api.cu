@@ -1064,8 +1064,10 @@ qlora_status qlora_linear_bwd_accumulate(const void* dY, const void* X, const vo
 
 // ---------------------------------------------------------------------------
 // XA = X A with scratch in a static device array (for callers that cannot
-// allocate the workspace).  Same kernels, same split count and tile order as
-// the forward's XA step, so the result equals qlora_linear_fwd's XA_save.
+// allocate the workspace).  The split partial sums go through the array and
+// a separate reduction kernel; the split count is the forward's (xa_splits)
+// and both sum the splits in split order from zero, so the result equals
+// qlora_linear_fwd's XA_save, which sums on chip.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) uint8_t g_xa_static_scratch[QLORA_XA_STATIC_SCRATCH_BYTES];
 
