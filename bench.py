@@ -166,8 +166,7 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-PAIR_PROFILE = os.path.join(ROOT, "profiles", "gemm_pair_llama3-8b-mlp.md")
-DEFAULT_WORKLOAD = "llama3-8b-mlp-m8192-4096x14336-r64"
+PAIR_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_pair_traffic.json")
 
 
 def pair_sources_sha256() -> str:
@@ -187,22 +186,24 @@ def pair_sources_sha256() -> str:
 
 
 def pair_traffic(workload: str):
-    """(bytes per launch, note): the ncu DRAM bytes committed under profiles/
-    for this workload's pair-GEMM launches, while the sources still match the
-    capture; else (None, why)."""
-    if workload != DEFAULT_WORKLOAD:
-        return None, "captured for the Llama-3-8B MLP workload only"
+    """(bytes per launch, note): the stored ncu capture of the pair GEMM's DRAM
+    bytes (a figure taken by an earlier ncu run, not by this run), reported
+    only for the workload it was taken on and while the sources still hash to
+    the captured state; else (None, why)."""
     try:
-        with open(PAIR_PROFILE) as fh:
-            text = fh.read()
-        val = int(text.split("traffic_bytes_per_launch:")[1].split()[0])
-        sha = text.split("sources_sha256:")[1].split()[0]
-    except (OSError, IndexError, ValueError):
-        return None, "no capture under profiles/"
+        with open(PAIR_TRAFFIC) as fh:
+            d = json.load(fh)
+        val = int(d["traffic_bytes_per_launch"])
+        sha = str(d["sources_sha256"])
+        wl = str(d["workload"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None, "no stored capture"
+    if workload != wl:
+        return None, f"stored capture is for the {wl} workload only"
     if sha != pair_sources_sha256():
-        return None, "kernel or tile order changed since the ncu capture under profiles/"
-    return val, ("ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, averaged over the step's "
-                 "six pair-GEMM launches; profiles/gemm_pair_llama3-8b-mlp.md")
+        return None, "kernel or tile order changed since the stored ncu capture"
+    return val, ("stored ncu capture (not measured by this run): " + d.get("what", "") +
+                 f"; {os.path.relpath(PAIR_TRAFFIC, ROOT)}")
 
 
 def run_ours(args, rank, world):
@@ -304,9 +305,11 @@ def run_ours(args, rank, world):
     binding.qlora_profiler_collect()
     prof_steps = max(1, min(args.steps, 50))
     torch.cuda.synchronize()
+    pt0 = time.perf_counter()
     for _ in range(prof_steps):
         step()
     torch.cuda.synchronize()
+    prof_ms = (time.perf_counter() - pt0) * 1e3
     kstats = binding.qlora_profiler_collect()
     binding.qlora_profiler_enable(False)
     st = binding.qlora_check_device_error(ws)
@@ -315,6 +318,32 @@ def run_ours(args, rank, world):
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
     value = flops * world / (ms_step * 1e-3) / 1e12
+
+    # ---- the same step with L2 flushed before each one (every input cold) ----
+    # The main figure needs no flush (each linear's X and dY, 67-235 MB, are
+    # larger than the 129 MB L2); this one also evicts the weights and the
+    # adapters: a 256 MB buffer is written before every step, outside the
+    # events that time the step.
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    fl_steps = max(3, min(args.steps, 30))
+    fl_ev = []
+    for _ in range(fl_steps):
+        flush.fill_(1)
+        fa, fb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fa.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+        fb.record(stream)
+        fl_ev.append((fa, fb))
+    torch.cuda.synchronize()
+    fl_ms = statistics.median(a.elapsed_time(b) for a, b in fl_ev)
+    fl_ms = max_over_ranks(fl_ms, world)
+    del flush
+    l2f = {"value": round(flops * world / (fl_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "ms_per_step": round(fl_ms, 4), "steps": fl_steps,
+           "how": "median of single steps, each preceded by a 256 MB write (2x L2) outside its CUDA events"}
 
     # ---- roofline of the dominant kernel (the tcgen05 base GEMM) ----
     peaks, peak_src = measured_peaks()
@@ -326,25 +355,33 @@ def run_ours(args, rank, world):
     main_ms = sum(ktimes.get(k, (0, 0.0))[1] for k in ("gemm_fwd", "gemm_dx"))
     main_launches = sum(ktimes.get(k, (0, 0.0))[0] for k in ("gemm_fwd", "gemm_dx"))
     achieved = main_flops_step * prof_steps / (main_ms * 1e-3) / 1e12 if main_ms > 0 else None
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
     traffic, traffic_note = pair_traffic(args.workload)
-    # A, B (dequantised weight) and C once per launch, averaged over the step's launches
-    alg_bytes = sum(2 * (li.M * li.K + li.N * li.K + li.M * li.N) * 2 for li in lins) / (2 * len(lins))
+    # A, B and C once per launch, averaged over the step's launches: with the
+    # bf16 dequantised weight the kernel reads (2 B per weight), and with the
+    # stored 4-bit weight (codes 0.5 B + absmax 4/64 B per weight)
+    nl2 = 2 * len(lins)
+    alg_bytes = sum(2 * (2 * li.M * li.K + 2 * li.N * li.K + 2 * li.M * li.N) for li in lins) / nl2
+    alg_bytes_4bit = sum(2 * (2 * li.M * li.K + li.N * li.K * (0.5 + 4 / 64) + 2 * li.M * li.N) for li in lins) / nl2
     roofline = {
         "kernel": "gemm_pair_kernel (forward Y and backward dX instances)",
         "bound": "tensor",
         "achieved": round(achieved, 2) if achieved else None,
         "peak": peak,
-        "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+        "peak_source": f"{peak_src} bf16_tflops (burst: a cuBLAS bf16 GEMM timed alone)",
         "unit": "TFLOP/s",
         "frac": round(achieved / peak, 4) if achieved else None,
+        "frac_sustained": round(achieved / peak_sus, 4) if achieved else None,
+        "peak_sustained": peak_sus,
         "traffic": traffic,
         "traffic_note": traffic_note,
         "algorithmic_bytes_per_launch": int(alg_bytes),
+        "algorithmic_bytes_per_launch_4bit_weight": int(alg_bytes_4bit),
         "launches": main_launches,
         "avg_launch_ms": round(main_ms / max(1, main_launches), 4),
-        "timing": f"CUDA events around each launch on the launching stream, {prof_steps} steps run "
-                  "right after the timed region",
+        "timing": f"CUDA events around each launch on the launching stream, {prof_steps} steps "
+                  f"({prof_ms / 1e3:.2f} s) run right after the timed region",
     }
     total_kernel_ms = sum(ms for _, _, ms in kstats)
     breakdown = {name: {"launches": n, "ms_per_step": round(ms / prof_steps, 4),
@@ -497,7 +534,8 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded numpy PCG64; shapes and value distributions of the pages' workloads)",
         "config": config_of(args.workload, lins, world),
         "pct_of_bf16_peak": round(100.0 * value / world / peak, 2),
-        "pct_of_bf16_peak_burst": round(100.0 * value / world / float(peaks.get("bf16_tflops", peak)), 2),
+        "pct_of_bf16_peak_sustained": round(100.0 * value / world / peak_sus, 2),
+        "l2_flushed": l2f,
         "roofline": roofline,
         "kernels": breakdown,
         "gpu_launches": int(launches),
@@ -530,6 +568,40 @@ def oracle_sample_run(lins, rows_per_linear):
     return flops, time.perf_counter() - t0
 
 
+def host_cpu() -> dict:
+    """The host's cores as the OS reports them (nproc, lscpu)."""
+    info = {"nproc": len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count(),
+            "logical_cpus": os.cpu_count()}
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            key, _, val = line.partition(":")
+            key = key.strip()
+            if key in ("Architecture", "Model name", "Socket(s)", "Core(s) per socket", "Thread(s) per core"):
+                info[key.lower().replace("(s)", "s").replace(" ", "_")] = val.strip()
+    except (OSError, subprocess.SubprocessError):
+        info["lscpu"] = "unavailable"
+    return info
+
+
+def oracle_single_thread():
+    """The oracle on one core: the tiny workload in full and a row sample of
+    the Llama-3-8B q_proj workload (GFLOP/s, dequant included in the time)."""
+    import oracle
+    nt = oracle.num_threads()
+    out = {}
+    try:
+        oracle.set_num_threads(1)
+        for name, rows in (("tiny-m256-k1024-n1024-r8", 256), ("llama3-8b-q_proj-m4096-k4096-n4096-r16", 16)):
+            lins = synth.workload(name, seed=0)
+            f, t = oracle_sample_run(lins, rows)
+            out[name] = {"rows": min(rows, lins[0].M), "of": lins[0].M, "gflop": round(f / 1e9, 3),
+                         "seconds": round(t, 3), "gflops": round(f / t / 1e9, 3)}
+    finally:
+        oracle.set_num_threads(nt)
+    return out
+
+
 def cpu_baseline(lins, target_s):
     import oracle
     oracle.build()
@@ -545,7 +617,7 @@ def cpu_baseline(lins, target_s):
     return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"fwd+bwd of every linear on its first {rows} tokens (of {lins[0].M}); "
                       f"{f / 1e9:.1f} GFLOP in {t:.1f} s, fp64, dequant included in the time",
-            "seconds": round(t, 2)}
+            "seconds": round(t, 2), "host": host_cpu(), "single_thread": oracle_single_thread()}
 
 
 def run_reference(args, rank, world):
@@ -576,7 +648,7 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(args.workload, lins, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "host": host_cpu()},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

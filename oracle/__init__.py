@@ -70,6 +70,8 @@ def _load():
             lib.oracle_backward_db.argtypes = [P, P, P, I, I, I, I, I, P, D, P, I, P, I, P]
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_num_threads.argtypes = []
+            lib.oracle_set_num_threads.restype = None
+            lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -84,6 +86,12 @@ def _c(a, dtype) -> np.ndarray:
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Worker threads of the following calls (timing only; results do not
+    depend on it: every output is one thread's ascending-order sum)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 # --------------------------------------------------------------------------

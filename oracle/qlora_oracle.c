@@ -297,10 +297,13 @@ void oracle_backward_db(const double *X, const double *dY, const double *A,
     free(xacol);
 }
 
-/* Number of worker threads the OpenMP runtime will use (1 without OpenMP). */
+/* Number of worker threads the OpenMP runtime will use (1 without OpenMP),
+ * and a way to change it (the benchmark also times the oracle on one core). */
 #ifdef _OPENMP
 #include <omp.h>
 int oracle_num_threads(void) { return omp_get_max_threads(); }
+void oracle_set_num_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
 #else
 int oracle_num_threads(void) { return 1; }
+void oracle_set_num_threads(int n) { (void)n; }
 #endif

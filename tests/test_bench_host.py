@@ -1,6 +1,7 @@
 """Host-side checks of bench.py's bookkeeping (no GPU): the FLOP count of the
-default workload, and the DRAM-traffic figure it reports from the committed
-ncu capture only while the captured sources are unchanged."""
+default workload, the DRAM-traffic figure it reports from the stored ncu
+capture only while the captured sources are unchanged, and the host-core
+description of the CPU baseline."""
 import bench
 from qlora_fine_tuning_gb300 import synth
 
@@ -16,20 +17,29 @@ def test_default_workload_flops():
 
 
 def test_traffic_reported_only_for_the_captured_sources():
+    import json
     val, note = bench.pair_traffic(bench.DEFAULT_WORKLOAD)
-    with open(bench.PAIR_PROFILE) as f:
-        matches = bench.pair_sources_sha256() in f.read()
-    if matches:   # the committed capture was taken with these sources
+    with open(bench.PAIR_TRAFFIC) as f:
+        matches = json.load(f)["sources_sha256"] == bench.pair_sources_sha256()
+    if matches:   # the stored capture was taken with these sources
         assert isinstance(val, int) and val > 0, note
+        assert "not measured by this run" in note
     else:         # the kernel changed since: no figure rather than a stale one
         assert val is None
     assert bench.pair_traffic("tiny-m256-k1024-n1024-r8")[0] is None
 
 
 def test_traffic_is_withdrawn_when_the_kernel_source_changes(tmp_path, monkeypatch):
-    text = open(bench.PAIR_PROFILE).read().replace(bench.pair_sources_sha256(), "0" * 64)
-    p = tmp_path / "profile.md"
-    p.write_text(text)
-    monkeypatch.setattr(bench, "PAIR_PROFILE", str(p))
+    import json
+    d = json.load(open(bench.PAIR_TRAFFIC))
+    d["sources_sha256"] = "0" * 64
+    p = tmp_path / "traffic.json"
+    p.write_text(json.dumps(d))
+    monkeypatch.setattr(bench, "PAIR_TRAFFIC", str(p))
     val, note = bench.pair_traffic(bench.DEFAULT_WORKLOAD)
     assert val is None and "changed" in note
+
+
+def test_host_cpu_reports_the_core_count():
+    info = bench.host_cpu()
+    assert info["nproc"] >= 1 and info["logical_cpus"] >= info["nproc"]

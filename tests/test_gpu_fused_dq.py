@@ -7,7 +7,7 @@ import pytest
 
 from qlora_fine_tuning_gb300 import binding, synth
 
-from harness import GpuLayer, compare, oracle_full, oracle_sampled, sample_indices
+from harness import GpuLayer, check_sampled, compare, oracle_full
 
 pytestmark = pytest.mark.gpu
 
@@ -49,16 +49,15 @@ def test_fused_dequant_matches_default_bitwise_and_oracle(M, N, K, r, s, seg, mo
 
 
 @pytest.mark.slow
-def test_fused_dequant_full_size_q_proj(monkeypatch):
-    label, kw = synth.WORKLOADS["llama3-8b-q_proj-m4096-k4096-n4096-r16"][0]
-    li = synth.make_linear(seed=0, stream=0, **kw)
-    got = _run(li, True, monkeypatch)
-    idx = sample_indices(li)
-    rows, kidx, Jidx, cidx, nidx = idx
-    ref = oracle_sampled(li, idx)
-    sub = {"Y": got["Y"][rows], "dX": got["dX"][rows], "XA": got["XA"][rows],
-           "dA": got["dA"][np.ix_(kidx, Jidx)], "dB": got["dB"][np.ix_(cidx, nidx)]}
-    compare(sub, ref, keys=("Y", "dX", "dA", "dB", "XA"))
+@pytest.mark.parametrize("name,which", [("llama3-8b-q_proj-m4096-k4096-n4096-r16", 0),
+                                        ("llama3-8b-mlp-m8192-4096x14336-r64", 2)])
+def test_fused_dequant_full_size(name, which, monkeypatch):
+    """Full size with the in-kernel expansion: the q_proj shape and the
+    Llama-3-8B down projection (K = 14336: the dX GEMM reads a column band of
+    the packed codes)."""
+    label, kw = synth.WORKLOADS[name][which]
+    li = synth.make_linear(seed=0, stream=which, **kw)
+    check_sampled(li, _run(li, True, monkeypatch))
 
 
 @pytest.mark.parametrize("label", ["gemm_fwd", "gemm_dx"])

@@ -11,8 +11,7 @@ import oracle
 from qlora_fine_tuning_gb300 import binding, synth
 
 from golden_case import expected_dense, load as load_golden
-from harness import (GpuLayer, TOL, compare, dev, host_bits, oracle_full, oracle_sampled,
-                     sample_indices)
+from harness import GpuLayer, TOL, check_sampled, compare, dev, host_bits, oracle_full
 
 pytestmark = pytest.mark.gpu
 
@@ -218,6 +217,7 @@ FULL = [
     ("llama3-8b-mlp-m8192-4096x14336-r64", 0),   # gate
     ("llama3-8b-mlp-m8192-4096x14336-r64", 2),   # down
     ("qwen3-14b-mlp-m16384-5120x17408-r16", 0),  # gate
+    ("qwen3-14b-mlp-m16384-5120x17408-r16", 2),  # down (K = 17408, N = 5120)
     ("llama3-8b-mlp-fused-gateup-m8192-4096x2x14336-r64", 0),  # gate and up as one two-adapter call
 ]
 
@@ -225,16 +225,63 @@ FULL = [
 @pytest.mark.slow
 @pytest.mark.parametrize("name,which", FULL)
 def test_full_size_sampled(name, which):
+    """Full size, in the launch configuration the benchmark times; the oracle
+    evaluates one row of every 256-row tile (all columns), one row of every
+    128-row block of dA and one column of every 128-column block of dB."""
     label, kw = synth.WORKLOADS[name][which]
     li = synth.make_linear(seed=0, stream=which, **kw)
     g = GpuLayer(li)
     g.forward()
     g.backward()
     g.check()
-    got = g.results()
-    idx = sample_indices(li)
-    rows, kidx, Jidx, cidx, nidx = idx
-    ref = oracle_sampled(li, idx)
-    sub = {"Y": got["Y"][rows], "dX": got["dX"][rows], "XA": got["XA"][rows],
-           "dA": got["dA"][np.ix_(kidx, Jidx)], "dB": got["dB"][np.ix_(cidx, nidx)]}
-    compare(sub, ref, keys=("Y", "dX", "dA", "dB", "XA"))
+    check_sampled(li, g.results())
+
+
+# --------------------------------------------------------------------------
+# stray writes: every output inside a canary-filled allocation
+# --------------------------------------------------------------------------
+
+PAD = 512  # elements before and after each output (keeps 16-byte alignment)
+
+
+def _canary(shape, dtype):
+    import torch
+    n = int(np.prod(shape))
+    if dtype == torch.bfloat16:
+        buf = torch.full((n + 2 * PAD,), 0x7FA5, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    else:
+        buf = torch.full((n + 2 * PAD,), 0x7FA5A5A5, dtype=torch.int32, device="cuda").view(torch.float32)
+    return buf, buf[PAD:PAD + n].view(*shape)
+
+
+def _pads_intact(buf):
+    import torch
+    raw = buf.view(torch.int16) if buf.dtype == torch.bfloat16 else buf.view(torch.int32)
+    want = 0x7FA5 if buf.dtype == torch.bfloat16 else 0x7FA5A5A5
+    head, tail = raw[:PAD], raw[-PAD:]
+    return bool((head == want).all()) and bool((tail == want).all())
+
+
+@pytest.mark.parametrize("M,N,K,r,seg", [(300, 264, 192, 16, None), (129, 520, 320, 8, (256, 264)),
+                                         (2304, 1032, 2304, 64, None)])
+def test_no_writes_outside_the_outputs(M, N, K, r, seg):
+    """Ragged M and N tails (partial row and column tiles, a partial last wave
+    of pair tiles): Y, XA, dX, dA and dB sit inside canary-filled buffers; the
+    canaries before and after each must be untouched and the outputs correct."""
+    import torch
+    li = synth.make_linear(M, N, K, r, 1.0, seg_n=seg, seed=M + K)
+    g = GpuLayer(li)
+    bufs = {}
+    for name, shape, dt in (("Y", (M, N), torch.bfloat16), ("XA", (M, li.R), torch.bfloat16),
+                            ("dX", (M, K), torch.bfloat16), ("dA", (K, li.R), torch.float32),
+                            ("dB", (r, N), torch.float32)):
+        buf, view = _canary(shape, dt)
+        bufs[name] = buf
+        setattr(g, name, view)
+    g.forward()
+    g.backward()
+    g.check()
+    torch.cuda.synchronize()
+    for name, buf in bufs.items():
+        assert _pads_intact(buf), f"a write landed outside {name}"
+    compare(g.results(), oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
