@@ -97,7 +97,13 @@ qlora_status dequant_4bit(const qlora_w4* w, void* out_bf16, float* out_f32, cud
 qlora_status quantize_4bit(const void* W, int32_t w_is_bf16, int64_t N, int64_t K, const float* codebook,
                            uint8_t* idx, float* absmax, cudaStream_t stream);
 
-/* Forward.  X bf16 [M,K]; A bf16 [K, n_seg*r]; B bf16 [r,N]; seg_n HOST int64
+/* Forward: XA = X A (saved for the backward), Y = X Wd^T + s (X A) B.
+ * Pages: "Introducing Unsloth: LLM 训练提速 30 倍", section 手动 Autograd (the
+ * adapted projection X(W + AB), bracketed through the rank-r side);
+ * "利用 Unsloth 和 NVIDIA 硬件加速 LLM 训练", section 1 (the 4-bit weight
+ * dequantised to 16 bits for the tensor-core product); "UnSloth极速微调" (the
+ * LoRA branch fused with the main linear).
+ * X bf16 [M,K]; A bf16 [K, n_seg*r]; B bf16 [r,N]; seg_n HOST int64
  * [n_seg] summing to N (may be NULL when n_seg == 1); s the LoRA scale.
  * Writes Y bf16 [M,N] and XA_save bf16 [M, n_seg*r] = bf16(X A) (pass it to
  * qlora_linear_bwd).  ws / ws_bytes: device workspace of at least
@@ -147,11 +153,13 @@ qlora_status qlora_check_device_error(void* ws, cudaStream_t stream);
 void qlora_set_wait_limit_ns(uint64_t ns);
 
 /* Test hook for the failure path: the next launch of the GEMM with this label
- * ("gemm_xa", "gemm_fwd", "gemm_g", "gemm_dx", "gemm_da" or "gemm_db")
+ * ("gemm_xa", "gemm_fwd", "gemm_g", "gemm_dx", "gemm_dadb" or
+ * "gemm_xa_static")
  * leaves the first shared-memory stage of its first CTA (CTA pair) unfilled,
  * so that CTA's consumer wait runs out after the wait limit; the kernel then
  * winds down, frees its tensor memory and sets the workspace error flag, and
- * qlora_check_device_error returns QLORA_ERR_TIMEOUT.  That call's outputs
+ * qlora_check_device_error (qlora_linear_xa_static_status for the
+ * static-scratch entry point) returns QLORA_ERR_TIMEOUT.  That call's outputs
  * are not valid; later calls work normally.  NULL clears a pending request. */
 void qlora_debug_stall_next_launch(const char* label);
 
@@ -184,21 +192,29 @@ uint64_t qlora_launch_counter(void);
  * same values qlora_linear_fwd writes to XA_save (R = n_seg * r there).
  * Its scratch is a static device array of QLORA_XA_STATIC_SCRATCH_BYTES
  * (8 MiB) that every GPU which loads the library holds until the process
- * exits.  The first call on a device looks the array's address up on that
- * device (make that first call before any stream capture).  All calls share
- * the array and it keeps the last call's contents: calls that can overlap on
- * the GPU (different streams, or several host threads) race -- order them on
- * one stream.  Nothing in the array has to start at zero.  The call
- * allocates nothing.  Sizes whose A^T (2 R K bytes) plus the fp32 partial
- * sums of 128 rows do not fit in the array are rejected with
- * QLORA_ERR_WORKSPACE (for example K = 16384 with R = 256); larger M is
- * processed in row chunks.  A device-side wait that runs out is not reported
- * by this entry point (XA is then unspecified).
+ * exits.  The first call on a device (and in each further CUDA context of
+ * that device) looks the array's address up with that device current; make
+ * that first call before any stream capture.  The cached address assumes the
+ * device is not reset while the library is loaded.  All calls share the array
+ * and it keeps the last call's contents: calls that can overlap on the GPU
+ * (different streams, or several host threads) race -- order them on one
+ * stream.  Only the array's failure word has to start at zero (it is zero
+ * when the library loads, and qlora_linear_xa_static_status clears it).  The
+ * call allocates nothing.  Sizes whose A^T (2 R K bytes) plus the fp32
+ * partial sums of 128 rows do not fit in the array (less a 256-byte header)
+ * are rejected with QLORA_ERR_WORKSPACE (for example K = 16384 with R = 256);
+ * larger M is processed in row chunks.
  * Preconditions: K % 64 == 0, 8 <= R <= 256, R % 8 == 0, 16-byte aligned
  * pointers.  Errors: INVALID_ARG, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA. */
 #define QLORA_XA_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
 qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t K, const void* A, int32_t R, void* XA,
                                     cudaStream_t stream);
+
+/* Device-side outcome of the qlora_linear_xa_static calls on the current
+ * device since the last query: synchronises `stream`, then returns OK,
+ * TIMEOUT (a kernel's bounded wait ran out; that call's XA is not valid) or
+ * CUDA, and clears the failure word.  Allocates nothing. */
+qlora_status qlora_linear_xa_static_status(cudaStream_t stream);
 
 #ifdef __cplusplus
 }

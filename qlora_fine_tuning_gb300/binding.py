@@ -95,6 +95,8 @@ def lib(path: Optional[str] = None):
             L.quantize_4bit.argtypes = [P, I32, I64, I64, P, P, P, P]
             L.qlora_linear_xa_static.restype = ctypes.c_int
             L.qlora_linear_xa_static.argtypes = [P, I64, I64, P, I32, P, P]
+            L.qlora_linear_xa_static_status.restype = ctypes.c_int
+            L.qlora_linear_xa_static_status.argtypes = [P]
             _lib = L
     return _lib
 
@@ -227,6 +229,12 @@ def qlora_linear_xa_static(X, M: int, K: int, A, R: int, XA, stream=None) -> Non
     cannot allocate device memory, so cannot provide a workspace."""
     st = lib().qlora_linear_xa_static(_ptr(X), int(M), int(K), _ptr(A), int(R), _ptr(XA), _stream(stream))
     _check(st, "qlora_linear_xa_static")
+
+
+def qlora_linear_xa_static_status(stream=None) -> int:
+    """Status of the static-scratch XA calls since the last query (OK or
+    TIMEOUT); clears it."""
+    return int(lib().qlora_linear_xa_static_status(_stream(stream)))
 
 
 # --------------------------------------------------------------------------

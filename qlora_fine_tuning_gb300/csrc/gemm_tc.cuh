@@ -95,8 +95,11 @@ struct GemmArgs {
   int32_t l2_hints;     // bit 0: streaming (evict-first) output stores;
                         // bit 1: the band's operand evict-last; bit 2: the other evict-first
   int32_t group_m;        // pair kernel tile order: >0 row tiles per band, <0 column tiles per band, 0 one band
-  const float* codebook;  // 16 fp32 values (pair kernel with in-kernel dequantisation)
-  int32_t dq_k;           // K of the 4-bit weight (pair kernel with in-kernel dequantisation)
+  // pair kernel with in-kernel dequantisation: the 4-bit weight [N, K]
+  const float* codebook;     // 16 fp32 values
+  const uint8_t* dq_idx;     // packed codes [N, K/2]
+  const float* dq_absmax;    // one scale per 64-block [N, K/64]
+  int32_t dq_k;              // K
   // EPI_RED outputs; `sum` is the full reduction, columns are shifted by out_col0:
   float red_scale;
   __nv_bfloat16* red_bf16;    // sum, row-major [row * red_ld + col]

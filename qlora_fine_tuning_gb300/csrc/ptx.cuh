@@ -183,6 +183,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Arrival on a barrier of another CTA of the cluster, ordered after this
+// thread's earlier writes at CTA scope.  For a hand-off whose data stays in
+// this CTA's shared memory and is read there by the tensor core (after a
+// proxy fence), this is the ordering needed; the cluster-scope release above
+// also waits for this thread's memory traffic to become visible cluster-wide,
+// which measured about 1 us per arrival.
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // 16-byte load from shared memory of a CTA of this cluster (cluster address).
 __device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
   float4 v;
@@ -477,6 +487,31 @@ __device__ __forceinline__ void tma_load_2d_pair_hint_ws(void* dst, const CUtens
       ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;\n\t}\n" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y), "l"(policy)
       : "memory");
+}
+
+}  // namespace qlora
+
+// ---------------------------------------------------------------------------
+// Asynchronous global -> shared copies (cp.async), completion tracked per
+// thread in commit groups.
+// ---------------------------------------------------------------------------
+namespace qlora {
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's most recent commit groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 }  // namespace qlora

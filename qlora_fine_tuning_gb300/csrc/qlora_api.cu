@@ -136,30 +136,6 @@ bool make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, in
   return r == CUDA_SUCCESS;
 }
 
-// 2-D map without swizzle for the packed codes (uint8) and absmax (fp32).
-bool make_map_plain(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int64_t inner, int64_t outer,
-                    int64_t ld_bytes, uint32_t box_inner, uint32_t box_outer) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_bytes)};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// Maps of the 4-bit weight for the pair kernel's in-kernel dequantisation.
-// Forward (B K-major): boxes of 128 output rows; dX (B MN-major): boxes of 64
-// reduction rows x 128 output columns.
-bool make_w4_maps(CUtensorMap* codes, CUtensorMap* scales, const qlora_w4* W, bool for_dx) {
-  const int64_t N = W->N, K = W->K;
-  const uint32_t rows = for_dx ? 64u : 128u;
-  return make_map_plain(codes, W->idx, CU_TENSOR_MAP_DATA_TYPE_UINT8, K / 2, N, K / 2, for_dx ? 64u : 32u, rows) &&
-         make_map_plain(scales, W->absmax, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, K / 64, N, (K / 64) * 4, 4u, rows);
-}
-
 // ---------------------------------------------------------------------------
 // Shapes, workspace
 // ---------------------------------------------------------------------------
@@ -553,30 +529,33 @@ bool pair_enabled() {
   return !(e && e[0] == '1');
 }
 
-// The pair kernel's in-kernel dequantisation runs on request
-// (QLORA_FUSED_DQ=1; slower than the standalone dequant on GB300) and needs
-// the absmax rows 16-byte strided (K % 256).
-bool fused_dq_ok(const qlora_w4* W) {
-  const char* e = std::getenv("QLORA_FUSED_DQ");
-  return e && e[0] == '1' && (W->K % 256 == 0);
+// In-kernel dequantisation in the pair GEMM (the 4-bit weight expanded into
+// the B tiles, no dequantised copy in the workspace).  QLORA_FUSED_DQ=1 turns
+// it on, =0 off.
+bool fused_dq_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("QLORA_FUSED_DQ");
+    return e && e[0] == '1';
+  }();
+  return on;
 }
 
 template <bool B_MN, bool FUSED>
 qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles, const CUtensorMap& a,
-                              const CUtensorMap& b, const CUtensorMap& a2, const CUtensorMap& b2,
-                              const CUtensorMap& sc, GemmArgs args, cudaStream_t st) {
+                              const CUtensorMap& b, const CUtensorMap& a2, const CUtensorMap& b2, GemmArgs args,
+                              cudaStream_t st) {
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  const int stages = FUSED ? 5 : kPairStages;
-  const size_t smem = size_t(stages) * (FUSED ? kPairDqStageBytes : kPairStageBytes) + 1024 + 512;
+  const int stages = kPairStages;
+  const size_t smem = size_t(stages) * kPairStageBytes + (FUSED ? kDqSlots * kDqSlotBytes : 0) + 1024 + 512;
   std::call_once(attr_once[dev & 63], [smem] {
     cudaFuncSetAttribute(gemm_pair_kernel<B_MN, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
   });
   args.bn = 256;
   args.stages = stages;
-  args.stage_bytes = FUSED ? kPairDqStageBytes : kPairStageBytes;
+  args.stage_bytes = kPairStageBytes;
   args.timeout_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   args.debug_stall = take_stall(name) ? 1 : 0;
   args.l2_hints = l2_hints();
@@ -588,8 +567,8 @@ qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles
   cudaError_t e;
   {
     LaunchScope ls(name, st);
-    e = launch_k(gemm_pair_kernel<B_MN, FUSED>, dim3(static_cast<unsigned>(2 * pairs)), dim3(FUSED ? 448 : 192),
-                 smem, st, a, b, a2, b2, sc, args);
+    e = launch_k(gemm_pair_kernel<B_MN, FUSED>, dim3(static_cast<unsigned>(2 * pairs)),
+                 dim3(FUSED ? 192 + 32 * kDqWarps : 192), smem, st, a, b, a2, b2, args);
   }
   return cuda_status(e);
 }
@@ -820,7 +799,7 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
   }
 
   // 2. Wd = deq(W), unless the pair GEMM dequantises in shared memory
-  const bool fused_fwd = pair_fwd && fused_dq_ok(W);
+  const bool fused_fwd = pair_fwd && fused_dq_enabled();
   if (!fused_fwd) QL_TRY(launch_dequant(W, Wd, nullptr, st));
 
   // 3. XA = X . A (A read MN-major; splits of K summed in the kernel);
@@ -851,12 +830,10 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     const int bn = b256 ? 256 : 128;
     const TileCfg tc = tile_cfg(bn);
     const uint32_t brows = pair ? 128u : static_cast<uint32_t>(bn);  // rows of B staged per CTA
-    CUtensorMap mSc;
     if (fused_fwd) {
-      if (!make_w4_maps(&mWd, &mSc, W, false)) return QLORA_ERR_CUDA;
+      mWd = mX;  // unused: the kernel reads the 4-bit weight itself
     } else {
       if (!make_map(&mWd, Wd, K, N, K, brows)) return QLORA_ERR_CUDA;
-      mSc = mWd;
     }
     if (!make_map(&mXAs, XAs, R, M, R, 128)) return QLORA_ERR_CUDA;
     if (pair ? !make_map(&mBt, B, N, r, N, 64) : !make_map(&mBt, Bt, L.Rp, N, L.Rp, brows)) return QLORA_ERR_CUDA;
@@ -874,12 +851,13 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     g.out_valid = static_cast<int32_t>(N);
     g.out = Y;
     g.codebook = W->codebook;
+    g.dq_idx = W->idx;
+    g.dq_absmax = W->absmax;
     g.dq_k = static_cast<int32_t>(K);
     if (fused_fwd) {
-      QL_TRY((launch_gemm_pair<false, true>("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, mSc, g, st)));
+      QL_TRY((launch_gemm_pair<false, true>("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, g, st)));
     } else if (pair) {
-      QL_TRY((launch_gemm_pair<false, false>("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, mSc, g,
-                                             st)));
+      QL_TRY((launch_gemm_pair<false, false>("gemm_fwd", cdiv(M, 256), cdiv(N, 256), mX, mWd, mXAs, mBt, g, st)));
     } else {
       dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(N, bn)), 1);
       QL_TRY((launch_gemm<false, false, EPI_BF16>("gemm_fwd", grid, tc, mX, mWd, mXAs, mBt, g, st)));
@@ -953,18 +931,16 @@ qlora_status linear_bwd(const void* dY, const void* X, const void* XA_saved, int
   // 2. dX = dY . Wd + (s G) . A^T
   if (dX) {
     const bool pair = pair_enabled();
-    const bool fused = pair && fused_dq_ok(W);
+    const bool fused = pair && fused_dq_enabled();
     const int bn = 256;
     const TileCfg tc = tile_cfg(bn);
-    CUtensorMap mSc;
     if (fused) {
       // the pair kernel expands the 4-bit codes into its MN-major B tiles
-      if (!make_w4_maps(&mWdT, &mSc, W, true)) return QLORA_ERR_CUDA;
+      mWdT = mdY;  // unused
     } else if (pair) {
       // row-major Wd [N,K], read MN-major by the pair kernel
       QL_TRY(launch_dequant(W, WdT, nullptr, st));
       if (!make_map(&mWdT, WdT, K, N, K, 64)) return QLORA_ERR_CUDA;
-      mSc = mWdT;
     } else {
       dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(cdiv(N, 64)));
       {
@@ -990,11 +966,13 @@ qlora_status linear_bwd(const void* dY, const void* X, const void* XA_saved, int
     g.out_valid = static_cast<int32_t>(K);
     g.out = dX;
     g.codebook = W->codebook;
+    g.dq_idx = W->idx;
+    g.dq_absmax = W->absmax;
     g.dq_k = static_cast<int32_t>(K);
     if (fused) {
-      QL_TRY((launch_gemm_pair<true, true>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, mSc, g, st)));
+      QL_TRY((launch_gemm_pair<true, true>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, g, st)));
     } else if (pair) {
-      QL_TRY((launch_gemm_pair<true, false>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, mSc, g, st)));
+      QL_TRY((launch_gemm_pair<true, false>("gemm_dx", cdiv(M, 256), cdiv(K, 256), mdY, mWdT, mGs, mA, g, st)));
     } else {
       dim3 grid(static_cast<unsigned>(cdiv(M, 128)), static_cast<unsigned>(cdiv(K, bn)), 1);
       QL_TRY((launch_gemm<false, false, EPI_BF16>("gemm_dx", grid, tc, mdY, mWdT, mGs, mA, g, st)));
@@ -1068,26 +1046,60 @@ qlora_status qlora_linear_bwd_accumulate(const void* dY, const void* X, const vo
 // a separate reduction kernel; the split count is the forward's (xa_splits)
 // and both sum the splits in split order from zero, so the result equals
 // qlora_linear_fwd's XA_save, which sums on chip.
+// Array layout: a 256-byte header whose first word collects device-side
+// failures (zero when the module loads, cleared by the status query), then
+// A^T [R, K] bf16, then the fp32 split partials of one row chunk.
 // ---------------------------------------------------------------------------
 static __device__ __align__(256) uint8_t g_xa_static_scratch[QLORA_XA_STATIC_SCRATCH_BYTES];
 
 namespace {
+constexpr size_t kStaticHeader = 256;
 std::mutex g_xa_static_mu;
-void* g_xa_static_addr[64] = {};
 
-// Device address of the static array on the current device, looked up once
-// per device with that device current.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The current CUDA context (driver entry point fetched through the runtime):
+// a module -- and with it the static array -- belongs to one context, so a
+// cached address is only valid for the context it was looked up in.
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+struct StaticAddr {
+  int dev;
+  CUcontext ctx;
+  void* addr;
+};
+std::vector<StaticAddr> g_xa_static_addr;
+
+// Device address of the static array in the current device's current
+// context, looked up (cudaGetSymbolAddress, with that device current) the
+// first time this device and context are seen.
 qlora_status xa_static_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QLORA_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return QLORA_ERR_UNSUPPORTED;
+  const CUcontext ctx = current_context();  // null before the runtime made one current: looked up again later
   std::lock_guard<std::mutex> lk(g_xa_static_mu);
-  if (!g_xa_static_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_xa_static_scratch) != cudaSuccess || !p) return QLORA_ERR_CUDA;
-    g_xa_static_addr[dev] = p;
-  }
-  *out = g_xa_static_addr[dev];
+  for (const StaticAddr& a : g_xa_static_addr)
+    if (a.dev == dev && a.ctx == ctx) {
+      *out = a.addr;
+      return QLORA_OK;
+    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_xa_static_scratch) != cudaSuccess || !p) return QLORA_ERR_CUDA;
+  g_xa_static_addr.push_back({dev, ctx, p});
+  *out = p;
   return QLORA_OK;
 }
 }  // namespace
@@ -1098,7 +1110,7 @@ extern "C" qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t
   if (M < 0 || K < 64 || R < 8 || R > 256 || R % 8 != 0) return QLORA_ERR_INVALID_ARG;
   if (K % 64 != 0 || K > (int64_t(1) << 30) || M > (int64_t(1) << 30)) return QLORA_ERR_UNSUPPORTED;
   if (!al16(X) || !al16(A) || !al16(XA)) return QLORA_ERR_ALIGNMENT;
-  const size_t cap = QLORA_XA_STATIC_SCRATCH_BYTES;
+  const size_t cap = QLORA_XA_STATIC_SCRATCH_BYTES - kStaticHeader;
   const int splits = xa_splits(M, K, R);
   const size_t at_bytes = align256(size_t(R) * K * 2);
   const size_t per_row = size_t(splits) * R * 4;
@@ -1110,8 +1122,9 @@ extern "C" qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t
   QL_TRY(xa_static_scratch(&base));
   if (!encode_fn()) return QLORA_ERR_CUDA;
   uint8_t* b8 = static_cast<uint8_t*>(base);
-  void* At = b8;
-  float* part = reinterpret_cast<float*>(b8 + at_bytes);
+  uint32_t* err = reinterpret_cast<uint32_t*>(b8);
+  void* At = b8 + kStaticHeader;
+  float* part = reinterpret_cast<float*>(b8 + kStaticHeader + at_bytes);
 
   {
     const TransposeJob jobs[1] = {tjob(A, K, R, R, At, R, K, K)};
@@ -1126,7 +1139,7 @@ extern "C" qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t
     const void* Xc = static_cast<const uint8_t*>(X) + size_t(m0) * K * 2;
     CUtensorMap mX;
     if (!make_map(&mX, Xc, K, mc, K, 128)) return QLORA_ERR_CUDA;
-    GemmArgs g = base_args(nullptr);
+    GemmArgs g = base_args(err);
     g.M = static_cast<int32_t>(mc);
     g.N = R;
     g.mode = GM_PLAIN;
@@ -1142,6 +1155,21 @@ extern "C" qlora_status qlora_linear_xa_static(const void* X, int64_t M, int64_t
     ra.out_bf16 = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(XA) + size_t(m0) * R * 2);
     ra.ld_o = R;
     QL_TRY(launch_reduce("reduce_xa_static", ra, st));
+  }
+  return QLORA_OK;
+}
+
+extern "C" qlora_status qlora_linear_xa_static_status(cudaStream_t st) {
+  void* base = nullptr;
+  QL_TRY(xa_static_scratch(&base));
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QLORA_ERR_CUDA;
+  uint32_t flag = 0;
+  if (cudaMemcpy(&flag, base, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return QLORA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return QLORA_ERR_CUDA;
+  if (flag != 0) {
+    if (cudaMemsetAsync(base, 0, 4, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+      return QLORA_ERR_CUDA;
+    return QLORA_ERR_TIMEOUT;
   }
   return QLORA_OK;
 }

@@ -10,7 +10,7 @@ import pytest
 import oracle
 from qlora_fine_tuning_gb300 import binding, synth
 
-from harness import TOL, GpuLayer, host_bits
+from harness import TOL, GpuLayer, compare, host_bits, oracle_operands
 
 pytestmark = pytest.mark.gpu
 
@@ -30,6 +30,21 @@ def _reference_xa(li):
     g.forward()
     g.check()
     return oracle.bf16_to_f64(host_bits(g.XA)[: li.M]), g
+
+
+def _oracle_xa(li):
+    X, Wd, A, B, _ = oracle_operands(li)
+    seg = None if len(li.seg_n) == 1 else li.seg_n
+    xa, _ = oracle.forward_rows(X, Wd, A, B, li.r, li.s, rows=list(range(li.M)), seg_n=seg)
+    return xa
+
+
+def _static_xa(li, g):
+    import torch
+    out = torch.empty((li.M, li.R), dtype=torch.bfloat16, device="cuda")
+    binding.qlora_linear_xa_static(g.X, li.M, li.K, g.A, li.R, out)
+    torch.cuda.synchronize()
+    return oracle.bf16_to_f64(host_bits(out))
 
 
 def test_static_scratch_xa_matches_forward_on_two_calls_in_a_row():
@@ -52,11 +67,44 @@ def test_static_scratch_xa_matches_forward_on_two_calls_in_a_row():
     assert oracle.rel_fro(got2, ref2) <= TOL
     # the same kernels, split count and tile order: identical values
     assert np.array_equal(got1, ref1) and np.array_equal(got2, ref2)
+    # and within the bound of the CPU oracle itself (tensor, every tile, every element)
+    compare({"XA": got1}, {"XA": _oracle_xa(li1)}, keys=("XA",))
 
     # calling again reuses the array, which still holds the last call's data
     binding.qlora_linear_xa_static(g1.X, li1.M, li1.K, g1.A, li1.R, out1)
     torch.cuda.synchronize()
     assert np.array_equal(oracle.bf16_to_f64(host_bits(out1)), ref1)
+    assert binding.qlora_linear_xa_static_status() == binding.OK
+
+
+# R = n_seg * r: 8 and 24 leave rows of the 16-row operand tile to the TMA zero
+# fill; 128 and 256 use other tile widths than the rank-64 cases above
+@pytest.mark.parametrize("M,N,K,r,seg", [(300, 256, 512, 8, None), (257, 320, 320, 8, (128, 128, 64)),
+                                         (384, 256, 1024, 128, None), (200, 384, 256, 128, (256, 128))])
+def test_static_scratch_xa_narrow_and_wide_ranks(M, N, K, r, seg):
+    li = synth.make_linear(M, N, K, r, 1.0, seg_n=seg, seed=M + r)
+    ref, g = _reference_xa(li)
+    got = _static_xa(li, g)
+    assert np.array_equal(got, ref)
+    compare({"XA": got}, {"XA": _oracle_xa(li)}, keys=("XA",))
+
+
+def test_static_scratch_reports_a_wait_that_ran_out():
+    """A stalled launch is reported by the status query (and only once); the
+    next call on the same context is correct."""
+    li = synth.make_linear(256, 256, 512, 16, 1.0, seed=35)
+    ref, g = _reference_xa(li)
+    binding.qlora_set_wait_limit_ns(50_000_000)
+    try:
+        binding.qlora_debug_stall_next_launch("gemm_xa_static")
+        _static_xa(li, g)
+        assert binding.qlora_linear_xa_static_status() == binding.TIMEOUT
+        assert binding.qlora_linear_xa_static_status() == binding.OK
+        assert np.array_equal(_static_xa(li, g), ref)
+        assert binding.qlora_linear_xa_static_status() == binding.OK
+    finally:
+        binding.qlora_debug_stall_next_launch(None)
+        binding.qlora_set_wait_limit_ns(2_000_000_000)
 
 
 def test_static_scratch_rejects_sizes_beyond_its_array():
