@@ -206,6 +206,85 @@ def pair_traffic(workload: str):
                  f"; {os.path.relpath(PAIR_TRAFFIC, ROOT)}")
 
 
+def reload_measure(layers, ws, ws_bytes, stream, reps=5):
+    """Backward pass of every linear with X and dY reloaded per layer through
+    LayerReload (1 and 2 buffer sets), and the per-layer copy and compute
+    times the pages' model takes."""
+    import torch
+    from qlora_fine_tuning_gb300 import binding
+    from qlora_fine_tuning_gb300.reload import LayerReload, model_double_buffer, model_single_buffer
+
+    def pinned(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    host = [[pinned(L["li"].X), pinned(L["li"].dY)] for L in layers]
+    order = list(reversed(range(len(layers))))
+    for L in layers:  # XA of every layer, resident
+        li = L["li"]
+        binding.qlora_linear_fwd(L["X"], li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["Y"], L["XA"], ws,
+                                 ws_bytes, stream)
+
+    def bwd(i, dev):
+        L = layers[i]
+        li = L["li"]
+        binding.qlora_linear_bwd(dev[1], dev[0], L["XA"], li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s,
+                                 L["dX"], L["dA"], L["dB"], ws, ws_bytes, stream)
+
+    def timed(fn, on=None):
+        s = stream if on is None else on
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    shapes = [[(L["li"].M, L["li"].K), (L["li"].M, L["li"].N)] for L in layers]
+    out = {}
+    for nbuf in (1, 2):
+        rl = LayerReload(shapes, torch.bfloat16, buffers=nbuf)
+        times = []
+        for _ in range(reps + 1):
+            def one():
+                start = torch.cuda.Event()
+                start.record(stream)
+                rl.copy_stream.wait_event(start)
+                rl.run(host, bwd, order=order, stream=stream)
+            times.append(timed(one))
+        out[nbuf] = statistics.median(times[1:])
+        del rl
+    # per-layer copy (alone, on a side stream) and compute (alone, inputs resident)
+    side = torch.cuda.Stream()
+    c_ms, g_ms = [], []
+    for i in order:
+        L = layers[i]
+        dX_, dY_ = torch.empty_like(L["X"]), torch.empty_like(L["dY"])
+        c_ms.append(statistics.median([_copy_time(side, dX_, dY_, host[i]) for _ in range(reps)]))
+        g_ms.append(statistics.median([timed(lambda: bwd(i, [L["X"], L["dY"]])) for _ in range(reps)]))
+        del dX_, dY_
+    h2d = sum(int(h.numel()) * 2 for pair in host for h in pair)
+    return {"what": "backward of every linear in reverse order, X and dY copied per layer from pinned host memory",
+            "t_single_ms": round(out[1], 4), "t_double_ms": round(out[2], 4),
+            "saved_ms": round(out[1] - out[2], 4),
+            "model_single_ms": round(model_single_buffer(c_ms, g_ms), 4),
+            "model_double_ms": round(model_double_buffer(c_ms, g_ms), 4),
+            "model_saved_ms": round(model_single_buffer(c_ms, g_ms) - model_double_buffer(c_ms, g_ms), 4),
+            "copy_ms": [round(v, 4) for v in c_ms], "compute_ms": [round(v, 4) for v in g_ms],
+            "h2d_bytes": h2d, "h2d_gbs": round(h2d / (sum(c_ms) * 1e-3) / 1e9, 1)}
+
+
+def _copy_time(side, d0, d1, host_pair):
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        a.record(side)
+        d0.copy_(host_pair[0], non_blocking=True)
+        d1.copy_(host_pair[1], non_blocking=True)
+        b.record(side)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
 def run_ours(args, rank, world):
     import torch
     from qlora_fine_tuning_gb300 import binding
@@ -477,6 +556,17 @@ def run_ours(args, rank, world):
         if st != binding.OK:
             raise RuntimeError(f"device error in e2e region: {binding.STATUS[st]}")
 
+    # ---- saved activations reloaded per layer (the pages' double buffer) ----
+    # The backward pass of every linear, in reverse order, with X and dY coming
+    # from pinned host memory through qlora_fine_tuning_gb300.reload (XA stays
+    # resident from a forward pass): one buffer set (copy, then compute) against
+    # two (the copy of the next layer under the compute of this one), beside
+    # the pages' model built from each layer's copy time c and compute time g
+    # measured alone.
+    reload_row = None
+    if not args.no_e2e:
+        reload_row = reload_measure(layers, ws, ws_bytes, stream)
+
     # ---- the storage step that feeds the path: GPU 4-bit quantisation ----
     # HBM-bound: reads 4 B (fp32 W) and writes 0.5 B of codes + 4/64 B of
     # absmax per weight.  Timed alone on the largest weight of the workload
@@ -543,6 +633,7 @@ def run_ours(args, rank, world):
         "clocks": clk,
         "e2e": e2e,
         "other_rows": other_rows,
+        "reload": reload_row,
     }
     return out, lins
 
