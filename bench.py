@@ -59,7 +59,9 @@ def config_of(name, lins, n_gpus):
         "linears": [{"label": li.meta.get("label"), "M": li.M, "K": li.K, "N": li.N, "r": li.r, "s": li.s,
                      "n_seg": len(li.seg_n)} for li in lins],
         "weights": "4-bit codebook indices + fp32 absmax per 64 (quantile codebook)",
-        "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
+        "parallelism": (f"data parallel x{n_gpus}: each rank its own {lins[0].M}-token shard per linear, "
+                        "W/A/B replicated, one sum all-reduce of dA and dB per linear on a reduce stream")
+                       if n_gpus > 1 else "single GPU",
         "l2": "inputs larger than L2 (per-step working set >> 129 MB), no flush",
     }
 
@@ -67,6 +69,22 @@ def config_of(name, lins, n_gpus):
 # --------------------------------------------------------------------------
 # distributed plumbing (barrier + max over ranks only)
 # --------------------------------------------------------------------------
+
+def relaunch(n_gpus: int) -> int:
+    """--gpus N > 1 without a launcher: start N ranks of this script under
+    torch.distributed.run on this node (one per GPU) and return its exit code."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    env = dict(os.environ)
+    env.setdefault("NCCL_DEBUG", "INFO")          # communicator set-up lines (ranks, nranks) on stderr
+    env.setdefault("NCCL_DEBUG_SUBSYS", "INIT")
+    env.setdefault("NCCL_DEBUG_FILE", "/dev/stderr")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n_gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd, env=env)
+
 
 def dist_init(n_gpus):
     rank = int(os.environ.get("RANK", "0"))
@@ -77,6 +95,9 @@ def dist_init(n_gpus):
         import torch
         if not torch.cuda.is_available():
             backend = "gloo"
+        os.environ.setdefault("NCCL_DEBUG", "INFO")
+        os.environ.setdefault("NCCL_DEBUG_SUBSYS", "INIT")
+        os.environ.setdefault("NCCL_DEBUG_FILE", "/dev/stderr")
         dist.init_process_group(backend=backend)
     return rank, world
 
@@ -288,10 +309,11 @@ def _copy_time(side, d0, d1, host_pair):
 def run_ours(args, rank, world):
     import torch
     from qlora_fine_tuning_gb300 import binding
+    from qlora_fine_tuning_gb300.dp import AdapterGradReducer, data_parallel_step
 
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     binding.lib()
-    lins = synth.workload(args.workload, seed=rank)
+    lins = synth.workload(args.workload, seed=0, shard=rank)
     M_all = sum(li.M for li in lins)
     flops = workload_flops(lins)
 
@@ -317,20 +339,24 @@ def run_ours(args, rank, world):
         layers.append(L)
     stream = torch.cuda.current_stream()
 
-    def step(Xs=None, dYs=None):
+    reducer = AdapterGradReducer() if world > 1 else None
+
+    def step():
         cur = torch.cuda.current_stream()  # the capture stream while a graph is recorded
-        for i, L in enumerate(layers):
-            li = L["li"]
-            X = L["X"] if Xs is None else Xs[i]
-            binding.qlora_linear_fwd(X, li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["Y"], L["XA"], ws,
-                                     ws_bytes, cur)
-        for i in reversed(range(len(layers))):
+
+        def fwd(i):
             L = layers[i]
             li = L["li"]
-            X = L["X"] if Xs is None else Xs[i]
-            dY = L["dY"] if dYs is None else dYs[i]
-            binding.qlora_linear_bwd(dY, X, L["XA"], li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["dX"],
-                                     L["dA"], L["dB"], ws, ws_bytes, cur)
+            binding.qlora_linear_fwd(L["X"], li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s, L["Y"], L["XA"],
+                                     ws, ws_bytes, cur)
+
+        def bwd(i):
+            L = layers[i]
+            li = L["li"]
+            binding.qlora_linear_bwd(L["dY"], L["X"], L["XA"], li.M, L["w"], L["A"], L["B"], li.r, L["seg"], li.s,
+                                     L["dX"], L["dA"], L["dB"], ws, ws_bytes, cur)
+
+        data_parallel_step(len(layers), fwd, bwd, lambda i: [layers[i]["dA"], layers[i]["dB"]], reducer)
 
     for _ in range(args.warmup):
         step()
@@ -344,7 +370,7 @@ def run_ours(args, rank, world):
     # host launch path from the timed region.
     graph = None
     per_step_launches = None
-    if not args.no_graph:
+    if not args.no_graph and world == 1:  # with ranks, the collectives run outside a graph
         c0 = binding.qlora_launch_counter()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
@@ -517,12 +543,16 @@ def run_ours(args, rank, world):
                     stream.wait_event(ev_back[i])   # previous dA/dB of this linear copied out
                 binding.qlora_linear_bwd(bufdY[b][i], bufX[b][i], L["XA"], li.M, L["w"], L["A"], L["B"], li.r,
                                          L["seg"], li.s, L["dX"], L["dA"], L["dB"], ws, ws_bytes, stream)
+                if reducer is not None:  # summed over the ranks before they go back to the host
+                    reducer.submit([L["dA"], L["dB"]], after=stream)
                 ev_bwd[i].record(stream)
                 fr = ev()
                 fr.record(stream)
                 ev_free[b][i] = fr
                 with torch.cuda.stream(down):
                     down.wait_event(ev_bwd[i])
+                    if reducer is not None:
+                        reducer.wait()  # the copy stream waits for the sums
                     hdA[i].copy_(L["dA"], non_blocking=True)
                     hdB[i].copy_(L["dB"], non_blocking=True)
                     bk = ev()
@@ -748,6 +778,8 @@ def main():
     args = parse()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch(args.gpus))
     rank, world = dist_init(args.gpus)
     if args.impl == "reference":
         out = run_reference(args, rank, world)

@@ -151,12 +151,18 @@ def make_linear(M: int, N: int, K: int, r: int, s: float, seg_n: Optional[Sequen
                 seed: int = 0, stream: int = 0, cb_kind: str = "Q",
                 x_std: float = 1.0, w_std: float = 0.02, b_std: float = 0.01,
                 dy_std: float = 0.01, w_zero: bool = False, a_zero: bool = False,
-                b_zero: bool = False, with_lengths: bool = False) -> LinearInputs:
+                b_zero: bool = False, with_lengths: bool = False, shard: int = 0) -> LinearInputs:
+    """One linear's seeded inputs.  `shard` > 0 draws X and dY (the tokens)
+    from a stream of their own, keeping W, A and B those of shard 0: the
+    token shard of one data-parallel rank."""
     seg = tuple(int(v) for v in (seg_n if seg_n is not None else (N,)))
     assert sum(seg) == N
     R = r * len(seg)
     ss = _seed_seq(seed, stream).spawn(6)
     g_w, g_x, g_a, g_b, g_dy, g_len = (np.random.Generator(np.random.PCG64(s_)) for s_ in ss)
+    if shard:
+        tx, tdy = np.random.SeedSequence([seed, stream, 1000 + shard]).spawn(2)
+        g_x, g_dy = np.random.Generator(np.random.PCG64(tx)), np.random.Generator(np.random.PCG64(tdy))
     cb = codebook(cb_kind)
     if w_zero:
         w = np.zeros((N, K), dtype=np.float32)
@@ -211,13 +217,14 @@ WORKLOADS = {
 }
 
 
-def workload(name: str, seed: int = 0, **overrides):
-    """All linears of a workload; linear i uses random stream i."""
+def workload(name: str, seed: int = 0, shard: int = 0, **overrides):
+    """All linears of a workload; linear i uses random stream i (`shard`: the
+    token shard of a data-parallel rank, see make_linear)."""
     out = []
     for i, (label, kw) in enumerate(WORKLOADS[name]):
         kw = dict(kw)
         kw.update(overrides)
-        li = make_linear(seed=seed, stream=i, **kw)
+        li = make_linear(seed=seed, stream=i, shard=shard, **kw)
         li.meta["label"] = label
         out.append(li)
     return out

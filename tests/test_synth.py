@@ -57,3 +57,11 @@ def test_flop_count_matches_the_definition():
     # 2MNK forward base + 2MNK dX base; three rank-r products on each side
     assert synth.flops_fwd_bwd(8192, 14336, 4096, 64) == 4 * 8192 * 14336 * 4096 + \
         6 * 8192 * 64 * (4096 + 14336)
+
+
+def test_token_shards_share_the_layer_and_differ_in_tokens():
+    a = synth.make_linear(16, 64, 64, 8, 1.0, seed=3)
+    b = synth.make_linear(16, 64, 64, 8, 1.0, seed=3, shard=1)
+    for k in ("idx", "absmax", "A", "B"):
+        assert np.array_equal(getattr(a, k), getattr(b, k)), k
+    assert not np.array_equal(a.X, b.X) and not np.array_equal(a.dY, b.dY)
