@@ -122,16 +122,53 @@ __device__ __forceinline__ int quant_code_exact(float v, float am, const double*
   return code;
 }
 
-constexpr int kQuantBuckets = 16384;  // table of the sorted-codebook quantiser (a multiple of 256)
+constexpr int kQuantBuckets = 16384;            // buckets of width 2/16384 over t in [-1, 1]
+constexpr int kQuantLut = kQuantBuckets + 16;    // entries 0..16384, padded
+constexpr float kQuantBias = 8396800.0f;         // 2^23 + 8192: fl(x + kQuantBias) has x rounded in its low bits
+
+__device__ __forceinline__ uint32_t bfi4(uint32_t field, uint32_t word, uint32_t pos) {
+  uint32_t d;
+  asm("bfi.b32 %0, %1, %2, %3, 4;" : "=r"(d) : "r"(field), "r"(word), "r"(pos));
+  return d;
+}
+
+// Sorted codebook, t32 next to a midpoint (its table bucket is not clear):
+// the number of midpoints below t32 by a branch-free binary search, confirmed
+// in double when t32 is within `margin` of a midpoint.  Out of line: a few
+// elements in a thousand come here, and the warp's main loop stays short.
+__device__ __noinline__ int quant_code_near(float t32, float v, float am, const float* mid, const double* cb64,
+                                            float margin) {
+  int code = (t32 > mid[7]) ? 8 : 0;
+  code += (t32 > mid[code + 3]) ? 4 : 0;
+  code += (t32 > mid[code + 1]) ? 2 : 0;
+  code += (t32 > mid[code]) ? 1 : 0;
+  const float lo = code > 0 ? fabsf(__fsub_rn(t32, mid[max(code - 1, 0)])) : INFINITY;
+  const float hi = code < 15 ? fabsf(__fsub_rn(mid[min(code, 14)], t32)) : INFINITY;
+  if (!(fminf(lo, hi) > margin)) code = quant_code_exact(v, am, cb64);
+  return code;
+}
+
+// Sorted codebook, absmax outside the range where the scaled reciprocal is
+// a normal float (or zero): the eight codes of a group by correctly rounded
+// division.
+__device__ __noinline__ uint32_t quant_group_divide(const float* v, float am, const float* mid, const double* cb64,
+                                                    float margin) {
+  uint32_t packed = 0;
+  for (int j = 0; j < 8; ++j) {
+    const float t32 = (am == 0.f) ? 0.f : __fdiv_rn(v[j], am);
+    packed = bfi4(static_cast<uint32_t>(quant_code_near(t32, v[j], am, mid, cb64, margin)), packed, 4u * j);
+  }
+  return packed;
+}
 
 template <bool BF16_IN>
-__global__ void __launch_bounds__(256) quantize4_kernel(const void* __restrict__ w,
+__global__ void __launch_bounds__(1024, 1) quantize4_kernel(const void* __restrict__ w,
                                                         const float* __restrict__ codebook, int64_t n_groups,
                                                         uint32_t* __restrict__ idx4, float* __restrict__ absmax) {
   __shared__ float cb[16];
   __shared__ float mid[15];
   __shared__ double cb64[16];
-  __shared__ int8_t lut[kQuantBuckets];
+  __shared__ int8_t lut[kQuantLut];
   griddep_wait();
   griddep_launch_dependents();
   if (threadIdx.x < 16) {
@@ -149,27 +186,6 @@ __global__ void __launch_bounds__(256) quantize4_kernel(const void* __restrict__
     if (i > 0 && !(cb[i - 1] < cb[i])) sorted = false;
   }
   const float margin = 1.0e-6f * (1.0f + cmax);
-  const float mid7 = mid[7];
-  // Sorted codebook: bucket b of t covers [-1 + b*h, -1 + (b+1)*h), h =
-  // 2/kQuantBuckets.  The bucket index computed from t32 is within 1.2e-7 of
-  // exact, so when no midpoint lies within 2*margin of the bucket every t32
-  // that lands in it has the bucket's code with the margin to spare; the
-  // entry holds that code, else -1 (binary search instead).  Each thread
-  // fills a contiguous run of buckets, walking the sorted midpoints once.
-  {
-    const float h = 2.0f / static_cast<float>(kQuantBuckets);
-    const int per = kQuantBuckets / static_cast<int>(blockDim.x);
-    const int b0 = static_cast<int>(threadIdx.x) * per;
-    int pm = 0;
-    for (int b = b0; b < b0 + per; ++b) {
-      const float lo = -1.0f + static_cast<float>(b) * h;
-      const float hi = lo + h;
-      while (pm < 15 && mid[pm] < lo - 2.0f * margin) ++pm;
-      const bool clear = sorted && (pm == 15 || mid[pm] > hi + 2.0f * margin);
-      lut[b] = clear ? static_cast<int8_t>(pm) : static_cast<int8_t>(-1);
-    }
-  }
-  __syncthreads();
   const int lane = threadIdx.x & 31;
   const unsigned grp_mask = 0xFFu << (lane & 24);  // the 8 lanes of this block
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;  // a multiple of 8
@@ -193,7 +209,40 @@ __global__ void __launch_bounds__(256) quantize4_kernel(const void* __restrict__
   };
   int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   float nx[8];
-  if (g < n_groups) load8(g, nx);
+  if (g < n_groups) load8(g, nx);  // in flight while the table is built
+  // Sorted codebook: bucket j (0..16384) covers t in [-1 + (j - 1/2) h,
+  // -1 + (j + 1/2) h), h = 2/16384.  The kernel takes j as the low bits of
+  // xb = fl(v * s8 + 2^23 + 8192), s8 = 8192 fl(1/am) (exact scaling): in
+  // [2^23, 2^24) the float grid is the integers, so xb is 8192 t' + 8192
+  // rounded to an integer, with t' = t (1 + d), |d| <= 2^-24 (the rounding
+  // of 1/am), t = v/am exact, |t| <= 1.  So 8192 t' is within 2^-11 of
+  // 8192 t, and the bucket found is t's own or a neighbour when t lies within
+  // 2^-11 / 8192 < 6.1e-8 of its edge.  Entry of a bucket, with its range
+  // widened by 2*margin on both sides (which covers that 6.1e-8):
+  //   k >= 0   no fp32 midpoint in the range: every t that can land here has
+  //            k midpoints below it, so code k, with the margin to spare;
+  //   ~k < 0   exactly one, midpoint k: code k + (t32 > mid[k]), settled in
+  //            fp32 when |t32 - mid[k]| > margin, else in double;
+  //   -128     several (a codebook with values closer than the bucket):
+  //            quant_code_near decides.
+  // Thread t fills buckets t, t + blockDim, ... (neighbouring threads write
+  // neighbouring bytes), walking the sorted midpoints once.
+  {
+    const float h = 2.0f / static_cast<float>(kQuantBuckets);
+    int pm = 0;
+    for (int b = static_cast<int>(threadIdx.x); b <= kQuantBuckets; b += static_cast<int>(blockDim.x)) {
+      const float lo = -1.0f + (static_cast<float>(b) - 0.5f) * h;
+      const float hi = lo + h;
+      while (pm < 15 && mid[pm] < lo - 2.0f * margin) ++pm;
+      int8_t e;
+      if (!sorted) e = -128;
+      else if (pm == 15 || mid[pm] > hi + 2.0f * margin) e = static_cast<int8_t>(pm);
+      else if (pm + 1 < 15 && mid[pm + 1] <= hi + 2.0f * margin) e = -128;
+      else e = static_cast<int8_t>(~pm);
+      lut[b] = e;
+    }
+  }
+  __syncthreads();
   for (; g < n_groups; g += stride) {
     // n_groups is a multiple of 8 and the 8 lanes of a block start 8-aligned,
     // so the 8 lanes of a block are all active here or all gone.
@@ -201,6 +250,10 @@ __global__ void __launch_bounds__(256) quantize4_kernel(const void* __restrict__
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = nx[j];
     if (g + stride < n_groups) load8(g + stride, nx);
+    if (g + 2 * stride < n_groups) {  // and the group after it towards L2
+      const char* pf = reinterpret_cast<const char*>(w) + (g + 2 * stride) * (BF16_IN ? 16 : 32);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(pf));
+    }
     float am = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) am = fmaxf(am, fabsf(v[j]));
@@ -209,27 +262,41 @@ __global__ void __launch_bounds__(256) quantize4_kernel(const void* __restrict__
     am = fmaxf(am, __shfl_xor_sync(grp_mask, am, 4, 8));
     uint32_t packed = 0;
     if (sorted) {
-      // 1/absmax is a normal float only inside this range (it overflows
-      // below ~2.9e-39 and loses precision as a subnormal above ~8.5e37):
-      // divide outside it
-      const bool by_rcp = am >= 1.0e-37f && am <= 1.0e37f;
-      const float inv = by_rcp ? __frcp_rn(am) : 0.f;
+      // 8192/absmax is a normal float inside this range; divide outside it
+      if (am >= 1.0e-33f && am <= 1.0e33f) {
+        const float s8 = __fmul_rn(__frcp_rn(am), 8192.0f);
+        int32_t neg = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float t32 = by_rcp ? __fmul_rn(v[j], inv) : (am == 0.f ? 0.f : __fdiv_rn(v[j], am));
-        const float xb = __fmaf_rn(t32, 0.5f * kQuantBuckets, 0.5f * kQuantBuckets);
-        int code = lut[min(max(static_cast<int>(xb), 0), kQuantBuckets - 1)];
-        if (code < 0) {
-          // number of midpoints below t32: branch-free binary search over the 15
-          code = (t32 > mid7) ? 8 : 0;
-          code += (t32 > mid[code + 3]) ? 4 : 0;
-          code += (t32 > mid[code + 1]) ? 2 : 0;
-          code += (t32 > mid[code]) ? 1 : 0;
-          const float lo = code > 0 ? fabsf(__fsub_rn(t32, mid[max(code - 1, 0)])) : INFINITY;
-          const float hi = code < 15 ? fabsf(__fsub_rn(mid[min(code, 14)], t32)) : INFINITY;
-          if (!(fminf(lo, hi) > margin)) code = quant_code_exact(v[j], am, cb64);
+        for (int j = 0; j < 8; ++j) {
+          const float xb = __fmaf_rn(v[j], s8, kQuantBias);
+          const int32_t code = lut[__float_as_int(xb) - 0x4B000000];
+          neg |= code;
+          packed = bfi4(static_cast<uint32_t>(code), packed, 4u * j);
         }
-        packed |= static_cast<uint32_t>(code) << (4 * j);
+        if (neg < 0) {  // an element next to a midpoint (one group in ~70)
+          const float inv = __fmul_rn(s8, 1.0f / 8192.0f);  // fl(1/am), exactly
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int32_t e = lut[__float_as_int(__fmaf_rn(v[j], s8, kQuantBias)) - 0x4B000000];
+            if (e >= 0) continue;
+            const float t32 = __fmul_rn(v[j], inv);
+            int code;
+            if (e == -128) {
+              code = quant_code_near(t32, v[j], am, mid, cb64, margin);
+            } else {
+              const int k = ~e;
+              const float d = __fsub_rn(t32, mid[k]);
+              code = k + (d > 0.f ? 1 : 0);
+              if (!(fabsf(d) > margin)) code = quant_code_exact(v[j], am, cb64);
+            }
+            packed = bfi4(static_cast<uint32_t>(code), packed, 4u * j);
+          }
+        }
+      } else {
+        float vs[8];  // only this rare branch takes an address (keeps v in registers)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) vs[j] = v[j];
+        packed = quant_group_divide(vs, am, mid, cb64, margin);
       }
     } else {
 #pragma unroll

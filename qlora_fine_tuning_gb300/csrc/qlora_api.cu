@@ -752,15 +752,15 @@ qlora_status quantize_4bit(const void* W, int32_t w_is_bf16, int64_t N, int64_t 
   if (!W || !codebook || !idx || !absmax) return QLORA_ERR_INVALID_ARG;
   if (!al16(W) || !al16(idx) || !al16(absmax)) return QLORA_ERR_ALIGNMENT;
   const int64_t groups = N * K / 8;
-  // one wave (4 CTAs of 256 per SM): each CTA builds its table once
-  const int64_t blocks = std::min<int64_t>(cdiv(groups, 256), int64_t(kSMs) * 4);
+  // one wave of one 1024-thread CTA per SM: each SM builds its table once
+  const int64_t blocks = std::min<int64_t>(cdiv(groups, 1024), int64_t(sm_count(cur_dev())));
   LaunchScope ls("quantize4", st);
   cudaError_t e;
   if (w_is_bf16)
-    e = launch_k(quantize4_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, W, codebook, groups,
+    e = launch_k(quantize4_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(1024), 0, st, W, codebook, groups,
                  reinterpret_cast<uint32_t*>(idx), absmax);
   else
-    e = launch_k(quantize4_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, W, codebook, groups,
+    e = launch_k(quantize4_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(1024), 0, st, W, codebook, groups,
                  reinterpret_cast<uint32_t*>(idx), absmax);
   return cuda_status(e);
 }
