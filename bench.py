@@ -190,19 +190,29 @@ def measured_peaks():
 PAIR_TRAFFIC = os.path.join(ROOT, "profiles", "gemm_pair_traffic.json")
 
 
-def pair_sources_sha256() -> str:
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and trailing blanks (string literals
+    in these files hold PTX, which has no comment markers)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
+def pair_sources_sha256(csrc: str = None) -> str:
     """sha256 of what decides the pair GEMM's DRAM traffic: its kernel source,
-    the PTX wrappers and the host's tile-order choice (pair_group())."""
+    the PTX wrappers and the host's tile-order choice (pair_group()), with
+    comments removed (a comment edit does not change the traffic)."""
     import hashlib
     import re
-    csrc = os.path.join(ROOT, "qlora_fine_tuning_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "qlora_fine_tuning_gb300", "csrc")
     h = hashlib.sha256()
     for f in ("gemm_pair.cuh", "ptx.cuh"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f)) as fh:
+            h.update(strip_comments(fh.read()).encode())
     with open(os.path.join(csrc, "qlora_api.cu")) as fh:
         m = re.search(r"int pair_group\(.*?\n}\n", fh.read(), re.S)
-    h.update(m.group(0).encode() if m else b"")
+    h.update(strip_comments(m.group(0)).encode() if m else b"")
     return h.hexdigest()
 
 

@@ -184,11 +184,13 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
 }
 
 // Arrival on a barrier of another CTA of the cluster, ordered after this
-// thread's earlier writes at CTA scope.  For a hand-off whose data stays in
-// this CTA's shared memory and is read there by the tensor core (after a
-// proxy fence), this is the ordering needed; the cluster-scope release above
-// also waits for this thread's memory traffic to become visible cluster-wide,
-// which measured about 1 us per arrival.
+// thread's earlier writes at CTA scope only.  Used by the opt-in in-kernel
+// dequantisation, whose tile stays in this CTA's shared memory and is read
+// there by the pair's tensor core after a proxy fence; the memory model asks
+// for cluster scope between threads of two CTAs, so this relies on the
+// hardware ordering the CTA's shared-memory writes before the remote arrival.
+// The cluster-scope release above waits for this thread's memory traffic to
+// become visible cluster-wide, which measured about 1 us per arrival.
 __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }

@@ -43,3 +43,16 @@ def test_traffic_is_withdrawn_when_the_kernel_source_changes(tmp_path, monkeypat
 def test_host_cpu_reports_the_core_count():
     info = bench.host_cpu()
     assert info["nproc"] >= 1 and info["logical_cpus"] >= info["nproc"]
+
+
+def test_traffic_survives_a_comment_edit_but_not_a_code_edit(tmp_path):
+    import shutil
+    src = tmp_path / "csrc"
+    shutil.copytree(bench.os.path.join(bench.ROOT, "qlora_fine_tuning_gb300", "csrc"), src)
+    base = bench.pair_sources_sha256(str(src))
+    p = src / "gemm_pair.cuh"
+    text = p.read_text()
+    p.write_text(text.replace("#pragma once", "// a new comment line\n#pragma once", 1))
+    assert bench.pair_sources_sha256(str(src)) == base
+    p.write_text(text.replace("kDqAhead = 4", "kDqAhead = 5", 1))
+    assert bench.pair_sources_sha256(str(src)) != base
