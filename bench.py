@@ -745,6 +745,7 @@ def cpu_baseline(lins, target_s):
     per_row = max((t2 - t1) / (r2 - r1), 1e-4)
     rows = int(max(r1, min(1024, r1 + (target_s - t1) / per_row)))
     f, t = oracle_sample_run(lins, rows)
+    rows = min(rows, lins[0].M)
     return {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"fwd+bwd of every linear on its first {rows} tokens (of {lins[0].M}); "
                       f"{f / 1e9:.1f} GFLOP in {t:.1f} s, fp64, dequant included in the time",
