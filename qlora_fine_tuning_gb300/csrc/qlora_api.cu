@@ -532,12 +532,10 @@ bool pair_enabled() {
 // In-kernel dequantisation in the pair GEMM (the 4-bit weight expanded into
 // the B tiles, no dequantised copy in the workspace).  QLORA_FUSED_DQ=1 turns
 // it on, =0 off.
+// Read on every call (not cached), so one process can run both paths.
 bool fused_dq_enabled() {
-  static const bool on = [] {
-    const char* e = std::getenv("QLORA_FUSED_DQ");
-    return e && e[0] == '1';
-  }();
-  return on;
+  const char* e = std::getenv("QLORA_FUSED_DQ");
+  return e && e[0] == '1';
 }
 
 template <bool B_MN, bool FUSED>

@@ -27,9 +27,15 @@ def _run(li, fused, monkeypatch):
     else:
         monkeypatch.delenv("QLORA_FUSED_DQ", raising=False)
     g = GpuLayer(li)
+    binding.qlora_profiler_enable(True)
+    binding.qlora_profiler_collect()
     g.forward()
     g.backward()
     g.check()
+    ran = {name for name, _, _ in binding.qlora_profiler_collect()}
+    binding.qlora_profiler_enable(False)
+    # the in-kernel path launches no separate dequantiser; the default does
+    assert ("dequant4" in ran) != fused, ran
     return g.results()
 
 
@@ -38,6 +44,9 @@ def _run(li, fused, monkeypatch):
     (300, 512, 512, 64, 0.25, None),              # ragged M
     (200, 1024, 512, 16, 1.0, (512, 256, 256)),   # three adapters
     (2048, 2560, 512, 16, 1.0, None),             # several tiles per CTA pair
+    (100, 136, 192, 16, 0.5, None),               # weight rows past N (Y) and reduction rows past N (dX)
+    (129, 264, 320, 8, 1.0, None),                # K = 320: dX output columns past K; K % 256 != 0
+    (257, 776, 448, 32, 2.0, (512, 264)),         # two adapters, ragged last segment, K % 256 != 0
 ])
 def test_fused_dequant_matches_default_bitwise_and_oracle(M, N, K, r, s, seg, monkeypatch):
     li = synth.make_linear(M, N, K, r, s, seg_n=seg, seed=M + N)

@@ -262,13 +262,20 @@ def _pads_intact(buf):
     return bool((head == want).all()) and bool((tail == want).all())
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("M,N,K,r,seg", [(300, 264, 192, 16, None), (129, 520, 320, 8, (256, 264)),
                                          (2304, 1032, 2304, 64, None)])
-def test_no_writes_outside_the_outputs(M, N, K, r, seg):
+def test_no_writes_outside_the_outputs(M, N, K, r, seg, fused, monkeypatch):
     """Ragged M and N tails (partial row and column tiles, a partial last wave
     of pair tiles): Y, XA, dX, dA and dB sit inside canary-filled buffers; the
-    canaries before and after each must be untouched and the outputs correct."""
+    canaries before and after each must be untouched and the outputs correct
+    -- with the dequantised weight read by TMA and with the 4-bit weight
+    expanded inside the GEMM."""
     import torch
+    if fused:
+        monkeypatch.setenv("QLORA_FUSED_DQ", "1")
+    else:
+        monkeypatch.delenv("QLORA_FUSED_DQ", raising=False)
     li = synth.make_linear(M, N, K, r, 1.0, seg_n=seg, seed=M + K)
     g = GpuLayer(li)
     bufs = {}
