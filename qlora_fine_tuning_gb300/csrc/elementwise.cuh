@@ -124,11 +124,6 @@ __device__ __forceinline__ int quant_code_exact(float v, float am, const double*
 
 constexpr int kQuantBuckets = 16384;            // buckets of width 2/16384 over t in [-1, 1]
 constexpr int kQuantLut = kQuantBuckets + 16;    // entries 0..16384, padded
-// Two copies of the table, the second shifted by 8 banks (16416 bytes = 4104
-// words apart); half-warp h reads copy h, so a warp's random lookups spread
-// over twice the banks (measured 75 -> 65 us; four copies measured the same).
-constexpr int kQuantLutStride = 16416;
-constexpr int kQuantLutCopies = 2;
 constexpr float kQuantBias = 8396800.0f;         // 2^23 + 8192: fl(x + kQuantBias) has x rounded in its low bits
 
 __device__ __forceinline__ uint32_t bfi4(uint32_t field, uint32_t word, uint32_t pos) {
@@ -173,7 +168,7 @@ __global__ void __launch_bounds__(1024, 1) quantize4_kernel(const void* __restri
   __shared__ float cb[16];
   __shared__ float mid[15];
   __shared__ double cb64[16];
-  __shared__ int8_t lut_copies[kQuantLutCopies * kQuantLutStride];
+  __shared__ int8_t lut[kQuantLut];
   griddep_wait();
   griddep_launch_dependents();
   if (threadIdx.x < 16) {
@@ -193,7 +188,6 @@ __global__ void __launch_bounds__(1024, 1) quantize4_kernel(const void* __restri
   const float margin = 1.0e-6f * (1.0f + cmax);
   const int lane = threadIdx.x & 31;
   const unsigned grp_mask = 0xFFu << (lane & 24);  // the 8 lanes of this block
-  const int8_t* lut = lut_copies + ((lane >> 4) & 1) * kQuantLutStride;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;  // a multiple of 8
   // Software pipelined: the next group's load is issued before the current
   // group is converted, so two loads per thread are in flight.
@@ -245,8 +239,7 @@ __global__ void __launch_bounds__(1024, 1) quantize4_kernel(const void* __restri
       else if (pm == 15 || mid[pm] > hi + 2.0f * margin) e = static_cast<int8_t>(pm);
       else if (pm + 1 < 15 && mid[pm + 1] <= hi + 2.0f * margin) e = -128;
       else e = static_cast<int8_t>(~pm);
-#pragma unroll
-      for (int c = 0; c < kQuantLutCopies; ++c) lut_copies[c * kQuantLutStride + b] = e;
+      lut[b] = e;
     }
   }
   __syncthreads();

@@ -110,6 +110,8 @@ SMALL = [
     # 81 pair tiles: one full wave of 76 pairs and a 5-tile tail
     (2304, 2304, 1024, 64, 0.25, (1280, 1024)),  # ... in the forward GEMM (two adapters)
     (2304, 1024, 2304, 16, 1.0, None),           # ... in the dX GEMM
+    (37, 8, 128, 8, 1.0, None),                  # the narrowest output: 8 columns of one tile
+    (96, 264, 192, 16, 0.0, None),               # s = 0: no adapter term; dA, dB exactly zero
 ]
 
 
@@ -123,6 +125,8 @@ def test_small_shapes_match_oracle(M, N, K, r, s, seg):
     got = g.results()
     ref = oracle_full(li)
     compare(got, ref, keys=("Y", "dX", "dA", "dB", "XA"))
+    if s == 0.0:
+        assert np.all(got["dA"] == 0.0) and np.all(got["dB"] == 0.0)
 
 
 @pytest.mark.parametrize("variant", ["w_zero", "b_large", "u_codebook"])
