@@ -38,8 +38,10 @@
 // call (dequant_4bit) and feeding bf16 tiles by TMA: with the expansion taken
 // out entirely (raw copies written instead) the hand-off through generic
 // shared-memory writes alone costs ~30%, and the expansion -- each weight is
-// expanded once per 256-row tile that uses it -- the rest.  The library runs
-// it only on request (QLORA_FUSED_DQ=1).
+// expanded once per 256-row tile that uses it -- the rest: its permutes,
+// logic ops and shifts run on the half-rate integer pipe, ~670 cycles of it
+// per CTA and stage against ~512 cycles for the stage's MMAs.  The library
+// runs it only on request (QLORA_FUSED_DQ=1).
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
