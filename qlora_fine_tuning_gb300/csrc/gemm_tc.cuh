@@ -88,6 +88,7 @@ struct GemmArgs {
   int32_t out_valid;    // columns n0+c >= out_valid are not stored
   int64_t out_split_stride;  // elements between split partial outputs
   int32_t m_tiles, n_tiles, z_tiles;  // tile grid (row tiles fastest)
+  int32_t tile_m;       // output rows per tile: 128, or (K-major A, EPI_RED) a multiple of 8 below it
   void* out;
   uint32_t* err;        // device error word (bit flags), may be null
   uint64_t timeout_ns;  // bound on every barrier wait
@@ -100,6 +101,9 @@ struct GemmArgs {
   const uint8_t* dq_idx;     // packed codes [N, K/2]
   const float* dq_absmax;    // one scale per 64-block [N, K/64]
   int32_t dq_k;              // K
+  // EPI_RED launch that also writes the bf16 Wd (epi_dequant_slice below):
+  __nv_bfloat16* dq_out;     // row-major [N, K]
+  int64_t dq_words;          // N*K/8 (8 weights each); 0 = no dequantisation in this launch
   // EPI_RED outputs; `sum` is the full reduction, columns are shifted by out_col0:
   float red_scale;
   __nv_bfloat16* red_bf16;    // sum, row-major [row * red_ld + col]
@@ -141,7 +145,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmArgs& p, int tile) {
   const int rest = tile / p.m_tiles;
   const int nt = rest % p.n_tiles;
   const int z = rest / p.n_tiles;
-  t.m0 = mt * 128;
+  t.m0 = mt * p.tile_m;
   t.n0 = nt * p.bn;
   t.split = z % p.splits;
   int sg = 0;
@@ -187,6 +191,97 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Dequantisation carried by a rank-r GEMM launch (XA in the forward, G in the
+// backward): while a CTA's producer and MMA warps stream X (or dY), its four
+// epilogue warps, idle until the accumulator is ready, expand one contiguous
+// slice of the 4-bit weight into the bf16 Wd; the producer and MMA warps join
+// once their own work is issued.  Both streams share one launch and keep HBM
+// busy together.  The arithmetic is the standalone dequantiser's:
+// deq = bf16_rn(fp32(codebook[code] * absmax)) with one __fmul_rn, so Wd is
+// the same bit for bit.
+// A word is 8 consecutive weights: one 4-byte load of codes, one absmax (8
+// words share a 64-block), one 16-byte bf16 store.  A unit is 32 x kDqUnroll
+// words, lane l taking words l, l + 32, ..., so that every warp load is 128
+// contiguous bytes and every warp store 512; warps claim units from a
+// shared-memory counter and load the next unit before converting the current
+// one.  Lane l holds codebook[l mod 16] and a lookup is one warp shuffle whose
+// source lane is the word shifted to the code (a shuffle reads only the low
+// five bits of its lane operand, and lanes l and l + 16 agree); all loop
+// bounds are warp-uniform so that every shuffle runs on the full warp.  The
+// two products of a byte come from one paired multiply (mul.rn.f32x2, each
+// half rounded to nearest like __fmul_rn).
+constexpr int kDqUnroll = 16;
+struct DqUnit {
+  uint32_t c[kDqUnroll];
+  float am[kDqUnroll];
+};
+
+__device__ __forceinline__ void dq_load(const GemmArgs& p, int64_t base, int64_t w1, int lane, DqUnit& u) {
+  const uint32_t* codes = reinterpret_cast<const uint32_t*>(p.dq_idx);
+#pragma unroll
+  for (int i = 0; i < kDqUnroll; ++i) {
+    const int64_t w = base + lane + 32 * i;
+    u.c[i] = w < w1 ? __ldg(codes + w) : 0u;
+    u.am[i] = w < w1 ? __ldg(p.dq_absmax + (w >> 3)) : 0.f;
+  }
+}
+
+// bf16 pair (lo, hi) = (bf16_rn(cl * am), bf16_rn(ch * am)); am2 = {am, am}.
+__device__ __forceinline__ uint32_t dq_pair(float cl, float ch, uint64_t am2) {
+  uint64_t c2, p2;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(c2) : "f"(cl), "f"(ch));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p2) : "l"(c2), "l"(am2));
+  float f0, f1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f0), "=f"(f1) : "l"(p2));
+  return pack_bf16x2(f0, f1);
+}
+
+__device__ __forceinline__ void dq_convert(const GemmArgs& p, int64_t base, int64_t w1, int lane, float cbv,
+                                           const DqUnit& u) {
+  uint4* out = reinterpret_cast<uint4*>(p.dq_out);
+#pragma unroll
+  for (int i = 0; i < kDqUnroll; ++i) {
+    const int64_t w = base + lane + 32 * i;
+    uint64_t am2;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(am2) : "f"(u.am[i]));
+    float c[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c[k] = __shfl_sync(0xFFFFFFFFu, cbv, static_cast<int>(u.c[i] >> (4 * k)));
+    const uint4 o = make_uint4(dq_pair(c[0], c[1], am2), dq_pair(c[2], c[3], am2), dq_pair(c[4], c[5], am2),
+                               dq_pair(c[6], c[7], am2));
+    if (w < w1) out[w] = o;
+  }
+}
+
+// One warp's share of this CTA's slice; `ctr` (shared memory, zeroed before
+// the roles start) hands out units.
+__device__ __noinline__ void dq_slice_warp(const GemmArgs& p, uint32_t* ctr, int lane) {
+  const float cbv = __ldg(p.codebook + (lane & 15));
+  const int64_t Wn = p.dq_words;
+  const int64_t per = (Wn + gridDim.x - 1) / gridDim.x;
+  const int64_t w0 = min(Wn, per * static_cast<int64_t>(blockIdx.x));
+  const int64_t w1 = min(Wn, w0 + per);
+  const int64_t unit = 32 * kDqUnroll;
+  const int64_t units = (w1 - w0 + unit - 1) / unit;
+  auto claim = [&]() -> int64_t {
+    uint32_t v = 0;
+    if (lane == 0) v = atomicAdd(ctr, 1u);
+    return static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, v, 0));
+  };
+  DqUnit cur, nxt;
+  int64_t k = claim();
+  if (k >= units) return;
+  dq_load(p, w0 + k * unit, w1, lane, cur);
+  while (true) {
+    const int64_t k2 = claim();
+    if (k2 < units) dq_load(p, w0 + k2 * unit, w1, lane, nxt);
+    dq_convert(p, w0 + k * unit, w1, lane, cbv, cur);
+    if (k2 >= units) break;
+    k = k2;
+    cur = nxt;
+  }
+}
+
 // Flat tile index of the T-th tile of a cluster walk (EPI_RED): the cluster
 // rank picks the split, z = segment * splits + split.
 __device__ __forceinline__ int red_tile(const GemmArgs& p, int T, uint32_t rank) {
@@ -218,6 +313,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* red_free = red_ready + 1;     // EPI_RED: this CTA's buffer read by all
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_free + 1);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  uint32_t* dq_ctr = reinterpret_cast<uint32_t*>(tmem_slot + 2);  // units of the Wd slice handed out
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -253,6 +349,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(red_free, static_cast<uint32_t>(S) * 128u);
     }
     *abort_flag = 0;
+    *dq_ctr = 0u;
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -287,7 +384,9 @@ __global__ void __launch_bounds__(192, 1)
       const CUtensorMap* mapA = second ? &tmA2 : &tmA;
       const CUtensorMap* mapB = second ? &tmB2 : &tmB;
       const TileInfo t = tile_info(pq, RED ? red_tile(pq, second ? T - tiles1 : T, rank) : T);
-      const uint32_t tx = kATileBytes + static_cast<uint32_t>(pq.bn) * 128u;
+      // A box: tile_m rows of 128 B (rows tile_m..127 of the stage keep stale
+      // bytes; they only feed accumulator rows the epilogue never stores).
+      const uint32_t tx = static_cast<uint32_t>(pq.tile_m + pq.bn) * 128u;
       for (int it = 0; it < t.n_iter; ++it) {
         const uint32_t s = g % static_cast<uint32_t>(p.stages);
         const uint32_t ph = (g / static_cast<uint32_t>(p.stages)) & 1u;
@@ -328,6 +427,7 @@ __global__ void __launch_bounds__(192, 1)
         ++g;
       }
     }
+    if (RED && p.dq_words > 0) dq_slice_warp(p, dq_ctr, lane);  // every copy is issued: help with Wd
     // Do not leave the CTA while copies it issued may still land in smem.
     if (lane == 0) {
       const uint32_t S_ = static_cast<uint32_t>(p.stages);
@@ -389,15 +489,14 @@ __global__ void __launch_bounds__(192, 1)
       tc_commit_ws(&tfull[acc]);  // arrives once this tile's MMAs have completed
     }
     tc_commit_ws(mma_done);
+    if (RED && p.dq_words > 0) dq_slice_warp(p, dq_ctr, lane);  // every MMA is issued: help with Wd
   } else if (warp >= 2 && RED) {
     // ---------------- Epilogue: sum the splits across the cluster ----------------
     if constexpr (RED) {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int et = static_cast<int>(threadIdx.x) - 64;  // 0..127
-    const int rs = (128 + S - 1) / S;                    // rows this CTA sums
-    const int lo = min(128, static_cast<int>(rank) * rs);
-    const int nrows = min(128, lo + rs) - lo;
+    if (p.dq_words > 0) dq_slice_warp(p, dq_ctr, lane);
     const uint32_t red_s = smem_u32(red);
     const uint32_t ready_s = smem_u32(red_ready);
     const uint32_t free_s = smem_u32(red_free);
@@ -418,6 +517,10 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after();
       const uint32_t t_base = tmem_base + acc * acc_cols + (static_cast<uint32_t>(q * 32) << 16);
+      // rows [lo, lo + nrows) of the tile's tile_m are this CTA's to sum
+      const int rs = (pq.tile_m + S - 1) / S;
+      const int lo = min(pq.tile_m, static_cast<int>(rank) * rs);
+      const int nrows = min(pq.tile_m, lo + rs) - lo;
       if (S == 1) {
         // One split: the accumulator is the sum; store straight from registers.
         const int grow = t.m0 + row;
@@ -430,7 +533,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) v[e] = 0u;
           }
-          if (grow >= pq.M) continue;
+          if (grow >= pq.M || row >= pq.tile_m) continue;
           const int gcol = t.n0 + c;
           const int lim = min(pq.out_valid, pq.N);
           if (pq.red_f32_t) {
@@ -599,7 +702,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after();
       const int grow = t.m0 + row;
-      const bool row_ok = grow < p.M;
+      const bool row_ok = grow < p.M && row < p.tile_m;
       const bool have_acc = t.n_iter > 0;
       const uint32_t t_base = tmem_base + acc * acc_cols + (static_cast<uint32_t>(q * 32) << 16);
       const int nchunks = p.bn / 16;

@@ -441,13 +441,29 @@ int red_splits(int64_t tiles, int64_t nkb, size_t smem) {
 }
 
 // One problem of a gemm_tc_kernel<.., EPI_RED> launch: tiles m_tiles x
-// n_tiles x zseg (zseg adapter segments for GM_G, else 1).
+// n_tiles x zseg (zseg adapter segments for GM_G, else 1) of g.tile_m rows.
 struct RedProb {
   GemmArgs g;
   CUtensorMap a, b;
   int64_t m_tiles, n_tiles, zseg;
   int bn;
 };
+
+// Row-tile height of a rank-r GEMM with a K-major A operand (XA, G) and
+// `splits` CTAs per tile: 128 rows, or -- when 128-row tiles leave clusters
+// of the wave unused -- the smallest multiple of 8 (at least 64) whose tiles
+// still fit in one wave, so that more SMs stream the operand.  Every row's
+// sum is over the same reduction chunks in the same order either way.
+// QLORA_RED_TILE_M=0 keeps 128 (read on every call).
+template <bool B_MN>
+int red_tile_m(int64_t M, int64_t zseg, int splits, size_t smem) {
+  const char* e = std::getenv("QLORA_RED_TILE_M");
+  if (e && e[0] == '0') return 128;
+  const int64_t per_seg = max_red_clusters<false, B_MN>(splits, smem) / std::max<int64_t>(zseg, 1);
+  if (per_seg <= cdiv(M, 128)) return 128;
+  const int64_t tm = std::max<int64_t>(64, rup(cdiv(M, per_seg), 8));
+  return (tm < 128 && cdiv(M, tm) > cdiv(M, 128)) ? static_cast<int>(tm) : 128;
+}
 
 // gemm_tc_kernel<.., EPI_RED>: `splits` CTAs per tile in one cluster; an
 // optional second problem shares the launch (its tiles follow the first's).
@@ -538,6 +554,24 @@ bool fused_dq_enabled() {
   return e && e[0] == '1';
 }
 
+// The row-major Wd written by the rank-r GEMM launch that precedes its use
+// (XA in the forward, G in the backward) instead of a dequantiser launch of
+// its own.  QLORA_DQ_IN_RANKR=0 launches the dequantiser separately (read on
+// every call).
+bool dq_in_rankr_enabled() {
+  const char* e = std::getenv("QLORA_DQ_IN_RANKR");
+  return !(e && e[0] == '0');
+}
+
+// Attach the dequantisation of W into the row-major Wd to a rank-r launch.
+void attach_dequant(GemmArgs& g, const qlora_w4* W, void* Wd) {
+  g.codebook = W->codebook;
+  g.dq_idx = static_cast<const uint8_t*>(W->idx);
+  g.dq_absmax = W->absmax;
+  g.dq_out = static_cast<__nv_bfloat16*>(Wd);
+  g.dq_words = W->N * W->K / 8;
+}
+
 template <bool B_MN, bool FUSED>
 qlora_status launch_gemm_pair(const char* name, int64_t m_tiles, int64_t n_tiles, const CUtensorMap& a,
                               const CUtensorMap& b, const CUtensorMap& a2, const CUtensorMap& b2, GemmArgs args,
@@ -576,6 +610,7 @@ GemmArgs base_args(uint32_t* err) {
   std::memset(&g, 0, sizeof(g));
   g.splits = 1;
   g.nseg = 1;
+  g.tile_m = 128;
   g.err = err;
   return g;
 }
@@ -798,17 +833,22 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
 
   // 2. Wd = deq(W), unless the pair GEMM dequantises in shared memory
   const bool fused_fwd = pair_fwd && fused_dq_enabled();
-  if (!fused_fwd) QL_TRY(launch_dequant(W, Wd, nullptr, st));
+  const bool dq_in_xa = !fused_fwd && dq_in_rankr_enabled();
+  if (!fused_fwd && !dq_in_xa) QL_TRY(launch_dequant(W, Wd, nullptr, st));
 
   // 3. XA = X . A (A read MN-major; splits of K summed in the kernel);
   //    writes XA_save = bf16(XA) and s*XA
   CUtensorMap mX, mWd, mXAs, mBt;
+  if (!make_map(&mX, X, K, M, K, 128)) return QLORA_ERR_CUDA;  // 128-row boxes of the base GEMM
   {
-    CUtensorMap mA;
+    CUtensorMap mA, mXr;
     const TileCfg tc = tile_cfg(static_cast<int>(rup(R, 64)), true);
     const int splits = xa_splits(M, K, R);
-    if (!make_map(&mX, X, K, M, K, 128) || !make_map(&mA, A, R, K, R, 64)) return QLORA_ERR_CUDA;
+    const int tm = red_tile_m<true>(M, 1, splits, tc.smem);
+    if (!make_map(&mXr, X, K, M, K, static_cast<uint32_t>(tm)) || !make_map(&mA, A, R, K, R, 64))
+      return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
+    g.tile_m = tm;
     g.M = static_cast<int32_t>(M);
     g.N = static_cast<int32_t>(R);
     g.mode = GM_PLAIN;
@@ -818,7 +858,8 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
     g.red_bf16 = reinterpret_cast<__nv_bfloat16*>(XA_save);
     g.red_bf16_s = reinterpret_cast<__nv_bfloat16*>(XAs);
     g.red_ld = R;
-    QL_TRY((launch_gemm_red<false, true>("gemm_xa", splits, tc, RedProb{g, mX, mA, cdiv(M, 128), 1, 1, tc.bn},
+    if (dq_in_xa) attach_dequant(g, W, Wd);  // the Wd of step 4
+    QL_TRY((launch_gemm_red<false, true>("gemm_xa", splits, tc, RedProb{g, mXr, mA, cdiv(M, tm), 1, 1, tc.bn},
                                          nullptr, st)));
   }
 
@@ -898,6 +939,11 @@ qlora_status linear_bwd(const void* dY, const void* X, const void* XA_saved, int
   void* G = w8 + L.off_g;
 
   CUtensorMap mdY, mB, mWdT, mGs, mA, mXmn, mGmn, mdYmn, mXAmn;
+  if (!make_map(&mdY, dY, N, M, N, 128)) return QLORA_ERR_CUDA;  // 128-row boxes of the base GEMM
+  // the pair dX reads the row-major Wd; the G launch writes it when enabled
+  const bool dx_pair = dX && pair_enabled();
+  const bool dx_fused = dx_pair && fused_dq_enabled();
+  const bool dq_in_g = dx_pair && !dx_fused && dq_in_rankr_enabled();
 
   // 1. G = dY . B^T per segment (splits of the segment's columns summed in
   //    the kernel); writes s*G and G
@@ -908,9 +954,12 @@ qlora_status linear_bwd(const void* dY, const void* X, const void* XA_saved, int
     int64_t min_nkb = INT64_MAX;
     for (int j = 0; j < n_seg; ++j) min_nkb = std::min<int64_t>(min_nkb, cdiv(sg.start[j + 1] - sg.start[j], 64));
     const int splits = red_splits<false, false>(mt * n_seg, min_nkb, tc.smem);
-    if (!make_map(&mdY, dY, N, M, N, 128) || !make_map(&mB, B, N, r, N, static_cast<uint32_t>(bn)))
+    const int tm = red_tile_m<false>(M, n_seg, splits, tc.smem);
+    CUtensorMap mdYr;
+    if (!make_map(&mdYr, dY, N, M, N, static_cast<uint32_t>(tm)) || !make_map(&mB, B, N, r, N, static_cast<uint32_t>(bn)))
       return QLORA_ERR_CUDA;
     GemmArgs g = base_args(err);
+    g.tile_m = tm;
     g.M = static_cast<int32_t>(M);
     g.N = r;
     g.mode = GM_G;
@@ -922,14 +971,15 @@ qlora_status linear_bwd(const void* dY, const void* X, const void* XA_saved, int
     g.red_bf16 = reinterpret_cast<__nv_bfloat16*>(G);
     g.red_bf16_s = reinterpret_cast<__nv_bfloat16*>(Gs);
     g.red_ld = R;
-    QL_TRY((launch_gemm_red<false, false>("gemm_g", splits, tc, RedProb{g, mdY, mB, mt, 1, n_seg, bn}, nullptr,
-                                          st)));
+    if (dq_in_g) attach_dequant(g, W, WdT);  // the row-major Wd of step 2
+    QL_TRY((launch_gemm_red<false, false>("gemm_g", splits, tc, RedProb{g, mdYr, mB, cdiv(M, tm), 1, n_seg, bn},
+                                          nullptr, st)));
   }
 
   // 2. dX = dY . Wd + (s G) . A^T
   if (dX) {
-    const bool pair = pair_enabled();
-    const bool fused = pair && fused_dq_enabled();
+    const bool pair = dx_pair;
+    const bool fused = dx_fused;
     const int bn = 256;
     const TileCfg tc = tile_cfg(bn);
     if (fused) {
@@ -937,7 +987,7 @@ qlora_status linear_bwd(const void* dY, const void* X, const void* XA_saved, int
       mWdT = mdY;  // unused
     } else if (pair) {
       // row-major Wd [N,K], read MN-major by the pair kernel
-      QL_TRY(launch_dequant(W, WdT, nullptr, st));
+      if (!dq_in_g) QL_TRY(launch_dequant(W, WdT, nullptr, st));
       if (!make_map(&mWdT, WdT, K, N, K, 64)) return QLORA_ERR_CUDA;
     } else {
       dim3 grid(static_cast<unsigned>(K / 64), static_cast<unsigned>(cdiv(N, 64)));

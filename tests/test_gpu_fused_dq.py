@@ -1,7 +1,14 @@
-"""The pair GEMM with the 4-bit weight expanded inside the kernel (opt-in,
-QLORA_FUSED_DQ=1).  Its expansion is the same fp32 product and bf16
-rounding as dequant_4bit and the MMA order is unchanged, so Y and dX must be
-bit-identical to the default path; everything must also meet the oracle bound."""
+"""Three ways to produce the bf16 weight the base GEMMs read:
+
+* "rankr" (default): the rank-r GEMM launch before each base GEMM (XA in the
+  forward, G in the backward) writes the row-major Wd from spare warps;
+* "separate" (QLORA_DQ_IN_RANKR=0): a dequantiser launch of its own;
+* "fused" (QLORA_FUSED_DQ=1): the pair GEMM expands the 4-bit weight into its
+  operand tiles, no Wd at all.
+
+All three are the same fp32 product and bf16 rounding as dequant_4bit and
+leave the MMA order unchanged, so Y, dX, dA, dB and XA must be bit-identical
+across them; each must also meet the oracle bound."""
 import numpy as np
 import pytest
 
@@ -21,11 +28,14 @@ def _cuda():
     yield
 
 
-def _run(li, fused, monkeypatch):
-    if fused:
-        monkeypatch.setenv("QLORA_FUSED_DQ", "1")
-    else:
-        monkeypatch.delenv("QLORA_FUSED_DQ", raising=False)
+MODES = {"rankr": {}, "separate": {"QLORA_DQ_IN_RANKR": "0"}, "fused": {"QLORA_FUSED_DQ": "1"}}
+
+
+def _run(li, mode, monkeypatch):
+    for k in ("QLORA_FUSED_DQ", "QLORA_DQ_IN_RANKR"):
+        monkeypatch.delenv(k, raising=False)
+    for k, v in MODES[mode].items():
+        monkeypatch.setenv(k, v)
     g = GpuLayer(li)
     binding.qlora_profiler_enable(True)
     binding.qlora_profiler_collect()
@@ -34,8 +44,8 @@ def _run(li, fused, monkeypatch):
     g.check()
     ran = {name for name, _, _ in binding.qlora_profiler_collect()}
     binding.qlora_profiler_enable(False)
-    # the in-kernel path launches no separate dequantiser; the default does
-    assert ("dequant4" in ran) != fused, ran
+    # only the "separate" mode launches the row-major dequantiser
+    assert ("dequant4" in ran) == (mode == "separate"), ran
     return g.results()
 
 
@@ -48,13 +58,13 @@ def _run(li, fused, monkeypatch):
     (129, 264, 320, 8, 1.0, None),                # K = 320: dX output columns past K; K % 256 != 0
     (257, 776, 448, 32, 2.0, (512, 264)),         # two adapters, ragged last segment, K % 256 != 0
 ])
-def test_fused_dequant_matches_default_bitwise_and_oracle(M, N, K, r, s, seg, monkeypatch):
+def test_weight_paths_match_bitwise_and_oracle(M, N, K, r, s, seg, monkeypatch):
     li = synth.make_linear(M, N, K, r, s, seg_n=seg, seed=M + N)
-    fused = _run(li, True, monkeypatch)
-    plain = _run(li, False, monkeypatch)
-    for k in ("Y", "dX", "dA", "dB", "XA"):
-        assert np.array_equal(fused[k], plain[k]), k
-    compare(fused, oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
+    res = {m: _run(li, m, monkeypatch) for m in MODES}
+    for m in ("separate", "fused"):
+        for k in ("Y", "dX", "dA", "dB", "XA"):
+            assert np.array_equal(res[m][k], res["rankr"][k]), (m, k)
+    compare(res["rankr"], oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
 
 
 @pytest.mark.slow
@@ -66,7 +76,7 @@ def test_fused_dequant_full_size(name, which, monkeypatch):
     the packed codes)."""
     label, kw = synth.WORKLOADS[name][which]
     li = synth.make_linear(seed=0, stream=which, **kw)
-    check_sampled(li, _run(li, True, monkeypatch))
+    check_sampled(li, _run(li, "fused", monkeypatch))
 
 
 @pytest.mark.parametrize("label", ["gemm_fwd", "gemm_dx"])
