@@ -634,20 +634,43 @@ def run_ours(args, rank, world):
     q_bytes = qli.N * qli.K * (4 + 0.5 + 4 / 64)
     q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
-    n_dq = ktimes.get("dequant4", (0, 0.0))
-    dq_bytes = sum(2 * li.N * li.K * 2.5625 for li in lins) * prof_steps  # fwd + bwd dequant per linear
+    # HBM-bound kernels of the step: algorithmic bytes (each operand read and
+    # each output written once) per step, against their event-timed duration.
+    # Without a dequant4 launch in the step, the bf16 Wd is written by the
+    # rank-r GEMM launch before each base GEMM (XA forward, G backward), and
+    # its expansion bytes (codes 0.5 + absmax 4/64 read, 2 written, per
+    # weight) count there.
+    wd_in_rankr = ktimes.get("dequant4", (0, 0.0))[0] == 0
+    wd_bytes = sum(li.N * li.K * (0.5 + 4 / 64 + 2) for li in lins)
+    hbm_bytes = {
+        "gemm_xa": sum(2 * li.M * li.K + 2 * li.K * li.R + 4 * li.M * li.R for li in lins)
+        + (wd_bytes if wd_in_rankr else 0),
+        "gemm_g": sum(2 * li.M * li.N + 2 * li.r * li.N + 4 * li.M * li.R for li in lins)
+        + (wd_bytes if wd_in_rankr else 0),
+        "gemm_dadb": sum(2 * li.M * li.K + 2 * li.M * li.N + 4 * li.M * li.R + 4 * li.K * li.R + 4 * li.r * li.N
+                         for li in lins),
+        "dequant4": 0 if wd_in_rankr else 2 * wd_bytes,
+    }
+    hbm_rows = {}
+    for name, b in hbm_bytes.items():
+        n, ms = ktimes.get(name, (0, 0.0))
+        if n == 0 or ms <= 0:
+            continue
+        gbs = b * prof_steps / (ms * 1e-3) / 1e9
+        hbm_rows[name] = {"launches_per_step": n // prof_steps, "algorithmic_bytes_per_step": int(b),
+                          "ms_per_step": round(ms / prof_steps, 4), "achieved": round(gbs, 1),
+                          "frac": round(gbs / hbm_peak, 4)}
+    hbm_ms = sum(ktimes.get(k, (0, 0.0))[1] for k in hbm_bytes)
     other_rows = {
         "quantize_4bit": {"shape": f"{qli.N}x{qli.K} fp32", "ms": round(q_ms, 4), "bound": "hbm",
                           "achieved": round(q_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                           "frac": round(q_gbs / hbm_peak, 4),
                           "algorithmic_bytes": int(q_bytes),
                           "timing": f"CUDA events around each of {q_reps} launches"},
-        "dequant_4bit": {"bound": "hbm", "launches": n_dq[0],
-                         "achieved": round(dq_bytes / (n_dq[1] * 1e-3) / 1e9, 1) if n_dq[1] > 0 else None,
-                         "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(dq_bytes / (n_dq[1] * 1e-3) / 1e9 / hbm_peak, 4) if n_dq[1] > 0 else None,
-                         "algorithmic_bytes_per_weight": 2.5625,
-                         "timing": "CUDA events around each launch inside the profiled steps"},
+        "hbm_bound_kernels": {"bound": "hbm", "peak": hbm_peak, "unit": "GB/s", "kernels": hbm_rows,
+                              "wd_written_by": "gemm_xa / gemm_g" if wd_in_rankr else "dequant4",
+                              "share_of_kernel_time": round(hbm_ms / total_kernel_ms, 4) if total_kernel_ms else None,
+                              "timing": "CUDA events around each launch inside the profiled steps"},
     }
     del Wq
 

@@ -556,11 +556,18 @@ bool fused_dq_enabled() {
 
 // The row-major Wd written by the rank-r GEMM launch that precedes its use
 // (XA in the forward, G in the backward) instead of a dequantiser launch of
-// its own.  QLORA_DQ_IN_RANKR=0 launches the dequantiser separately (read on
-// every call).
-bool dq_in_rankr_enabled() {
+// its own.  Measured on GB300 (whole step): faster at M = 8192 tokens
+// (Llama-3-8B MLP +1.2%, fused QKV +1.1%), even at 2x the weight or
+// M = 16384, slower at M = 4096 (q_proj -4.3%) and M = 256 (-6.8%), where the
+// separate dequantiser's small CTAs overlap the neighbouring launches better
+// than one launch of full-SM CTAs.  So: from 8192 tokens on.
+// QLORA_DQ_IN_RANKR=0 / =1 forces either way (read on every call).
+constexpr int64_t kDqInRankrMinM = 8192;
+bool dq_in_rankr_enabled(int64_t M) {
   const char* e = std::getenv("QLORA_DQ_IN_RANKR");
-  return !(e && e[0] == '0');
+  if (e && e[0] == '0') return false;
+  if (e && e[0] == '1') return true;
+  return M >= kDqInRankrMinM;
 }
 
 // Attach the dequantisation of W into the row-major Wd to a rank-r launch.
@@ -833,7 +840,7 @@ qlora_status qlora_linear_fwd(const void* X, int64_t M, const qlora_w4* W, const
 
   // 2. Wd = deq(W), unless the pair GEMM dequantises in shared memory
   const bool fused_fwd = pair_fwd && fused_dq_enabled();
-  const bool dq_in_xa = !fused_fwd && dq_in_rankr_enabled();
+  const bool dq_in_xa = !fused_fwd && dq_in_rankr_enabled(M);
   if (!fused_fwd && !dq_in_xa) QL_TRY(launch_dequant(W, Wd, nullptr, st));
 
   // 3. XA = X . A (A read MN-major; splits of K summed in the kernel);
@@ -943,7 +950,7 @@ qlora_status linear_bwd(const void* dY, const void* X, const void* XA_saved, int
   // the pair dX reads the row-major Wd; the G launch writes it when enabled
   const bool dx_pair = dX && pair_enabled();
   const bool dx_fused = dx_pair && fused_dq_enabled();
-  const bool dq_in_g = dx_pair && !dx_fused && dq_in_rankr_enabled();
+  const bool dq_in_g = dx_pair && !dx_fused && dq_in_rankr_enabled(M);
 
   // 1. G = dY . B^T per segment (splits of the segment's columns summed in
   //    the kernel); writes s*G and G

@@ -1,10 +1,13 @@
 """Three ways to produce the bf16 weight the base GEMMs read:
 
-* "rankr" (default): the rank-r GEMM launch before each base GEMM (XA in the
-  forward, G in the backward) writes the row-major Wd from spare warps;
-* "separate" (QLORA_DQ_IN_RANKR=0): a dequantiser launch of its own;
+* "rankr" (QLORA_DQ_IN_RANKR=1; the default from 8192 tokens on): the rank-r
+  GEMM launch before each base GEMM (XA in the forward, G in the backward)
+  writes the row-major Wd from spare warps;
+* "separate" (QLORA_DQ_IN_RANKR=0; the default below 8192 tokens): a
+  dequantiser launch of its own;
 * "fused" (QLORA_FUSED_DQ=1): the pair GEMM expands the 4-bit weight into its
-  operand tiles, no Wd at all.
+  operand tiles, no Wd at all (a forward that cannot use the pair GEMM takes
+  its Wd from the XA launch).
 
 All three are the same fp32 product and bf16 rounding as dequant_4bit and
 leave the MMA order unchanged, so Y, dX, dA, dB and XA must be bit-identical
@@ -28,7 +31,8 @@ def _cuda():
     yield
 
 
-MODES = {"rankr": {}, "separate": {"QLORA_DQ_IN_RANKR": "0"}, "fused": {"QLORA_FUSED_DQ": "1"}}
+MODES = {"rankr": {"QLORA_DQ_IN_RANKR": "1"}, "separate": {"QLORA_DQ_IN_RANKR": "0"},
+         "fused": {"QLORA_FUSED_DQ": "1", "QLORA_DQ_IN_RANKR": "1"}}
 
 
 def _run(li, mode, monkeypatch):
@@ -65,6 +69,26 @@ def test_weight_paths_match_bitwise_and_oracle(M, N, K, r, s, seg, monkeypatch):
         for k in ("Y", "dX", "dA", "dB", "XA"):
             assert np.array_equal(res[m][k], res["rankr"][k]), (m, k)
     compare(res["rankr"], oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
+
+
+@pytest.mark.parametrize("M,separate", [(4096, True), (8192, False)])
+def test_default_weight_path_follows_token_count(M, separate, monkeypatch):
+    """Without a switch, the separate dequantiser below 8192 tokens and the
+    Wd written by the rank-r launches from 8192 on; both within the oracle
+    bounds."""
+    for k in ("QLORA_FUSED_DQ", "QLORA_DQ_IN_RANKR"):
+        monkeypatch.delenv(k, raising=False)
+    li = synth.make_linear(M, 512, 256, 16, 1.0, seed=M + 3)
+    g = GpuLayer(li)
+    binding.qlora_profiler_enable(True)
+    binding.qlora_profiler_collect()
+    g.forward()
+    g.backward()
+    g.check()
+    ran = {name for name, _, _ in binding.qlora_profiler_collect()}
+    binding.qlora_profiler_enable(False)
+    assert ("dequant4" in ran) == separate, ran
+    compare(g.results(), oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
 
 
 @pytest.mark.slow
