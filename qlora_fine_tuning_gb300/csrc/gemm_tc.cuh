@@ -289,8 +289,16 @@ __device__ __forceinline__ int red_tile(const GemmArgs& p, int T, uint32_t rank)
   return T % mn + mn * ((T / mn) * p.splits + static_cast<int>(rank));
 }
 
+// EPI_RED launches carry kRedExtraWarps more warps (6 .. 11) whose only work
+// is the Wd slice (none when the launch writes no Wd), so that up to 12 warps
+// of a CTA keep code loads in flight.  Measured on the Llama-3-8B MLP step:
+// 2 extra warps took 26 us per step off XA + G, 4 and 6 a further 11 and
+// 2 us; 10 are slower (the registers a thread may hold fall to 128 and spill).
+constexpr int kRedExtraWarps = 6;
+constexpr int kRedThreads = 192 + 32 * kRedExtraWarps;
+
 template <bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kRedThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ GemmArgs p, const __grid_constant__ GemmArgs p2) {
@@ -490,6 +498,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     tc_commit_ws(mma_done);
     if (RED && p.dq_words > 0) dq_slice_warp(p, dq_ctr, lane);  // every MMA is issued: help with Wd
+  } else if (warp >= 6) {
+    // ---------------- EPI_RED: extra warps, Wd only ----------------
+    if (RED && p.dq_words > 0) dq_slice_warp(p, dq_ctr, lane);
   } else if (warp >= 2 && RED) {
     // ---------------- Epilogue: sum the splits across the cluster ----------------
     if constexpr (RED) {

@@ -404,7 +404,7 @@ int max_red_clusters(int splits, size_t smem) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(splits) * 64u);
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(kRedThreads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -510,7 +510,7 @@ qlora_status launch_gemm_red(const char* name, int splits, const TileCfg& tc_in,
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * splits));
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(kRedThreads);
   cfg.dynamicSmemBytes = tc.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
