@@ -556,9 +556,9 @@ bool fused_dq_enabled() {
 
 // The row-major Wd written by the rank-r GEMM launch that precedes its use
 // (XA in the forward, G in the backward) instead of a dequantiser launch of
-// its own.  Measured on GB300 (whole step): faster at M = 8192 tokens
-// (Llama-3-8B MLP +1.2%, fused QKV +1.1%), even at 2x the weight or
-// M = 16384, slower at M = 4096 (q_proj -4.3%) and M = 256 (-6.8%), where the
+// its own.  Measured on GB300 (whole step, interleaved): faster at M = 8192
+// tokens (Llama-3-8B MLP +2.3%, the two-adapter gate/up call +1.6%, fused QKV
+// +1.1%), slower at M = 4096 (q_proj -2.1%) and M = 256 (-6.8%), where the
 // separate dequantiser's small CTAs overlap the neighbouring launches better
 // than one launch of full-SM CTAs.  So: from 8192 tokens on.
 // QLORA_DQ_IN_RANKR=0 / =1 forces either way (read on every call).
