@@ -254,8 +254,11 @@ __device__ __forceinline__ void dq_convert(const GemmArgs& p, int64_t base, int6
 }
 
 // One warp's share of this CTA's slice; `ctr` (shared memory, zeroed before
-// the roles start) hands out units.
-__device__ __noinline__ void dq_slice_warp(const GemmArgs& p, uint32_t* ctr, int lane) {
+// the roles start) hands out units.  With `poll` (the split-sum warps: the
+// barrier of their first accumulator), the warp leaves after the current unit
+// once that phase has completed, so that the split exchange runs beside the
+// rest of the expansion instead of after it; it calls again afterwards.
+__device__ __noinline__ void dq_slice_warp(const GemmArgs& p, uint32_t* ctr, int lane, uint64_t* poll = nullptr) {
   const float cbv = __ldg(p.codebook + (lane & 15));
   const int64_t Wn = p.dq_words;
   const int64_t per = (Wn + gridDim.x - 1) / gridDim.x;
@@ -268,12 +271,18 @@ __device__ __noinline__ void dq_slice_warp(const GemmArgs& p, uint32_t* ctr, int
     if (lane == 0) v = atomicAdd(ctr, 1u);
     return static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, v, 0));
   };
+  auto ready = [&]() -> bool {
+    if (!poll) return false;
+    const bool r = lane == 0 && mbar_try_wait(poll, 0u);
+    return __shfl_sync(0xFFFFFFFFu, r ? 1 : 0, 0) != 0;
+  };
+  if (ready()) return;
   DqUnit cur, nxt;
   int64_t k = claim();
   if (k >= units) return;
   dq_load(p, w0 + k * unit, w1, lane, cur);
   while (true) {
-    const int64_t k2 = claim();
+    const int64_t k2 = ready() ? units : claim();
     if (k2 < units) dq_load(p, w0 + k2 * unit, w1, lane, nxt);
     dq_convert(p, w0 + k * unit, w1, lane, cbv, cur);
     if (k2 >= units) break;
@@ -507,7 +516,7 @@ __global__ void __launch_bounds__(kRedThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
     const int et = static_cast<int>(threadIdx.x) - 64;  // 0..127
-    if (p.dq_words > 0) dq_slice_warp(p, dq_ctr, lane);
+    if (p.dq_words > 0) dq_slice_warp(p, dq_ctr, lane, &tfull[0]);
     const uint32_t red_s = smem_u32(red);
     const uint32_t ready_s = smem_u32(red_ready);
     const uint32_t free_s = smem_u32(red_free);
@@ -695,6 +704,7 @@ __global__ void __launch_bounds__(kRedThreads, 1)
       if (!*abort_flag) report(p, 32u);
       *abort_flag = 1;
     }
+    if (p.dq_words > 0) dq_slice_warp(p, dq_ctr, lane);  // the rest of Wd, if any
     }  // if constexpr (RED)
   } else if (warp >= 2) {
     // ---------------- Epilogue ----------------
