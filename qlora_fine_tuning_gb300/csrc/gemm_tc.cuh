@@ -192,11 +192,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Dequantisation carried by a rank-r GEMM launch (XA in the forward, G in the
-// backward): while a CTA's producer and MMA warps stream X (or dY), its four
-// epilogue warps, idle until the accumulator is ready, expand one contiguous
-// slice of the 4-bit weight into the bf16 Wd; the producer and MMA warps join
-// once their own work is issued.  Both streams share one launch and keep HBM
-// busy together.  The arithmetic is the standalone dequantiser's:
+// backward): while a CTA's producer and MMA warps stream X (or dY), the rest
+// of the CTA expands one contiguous slice of the 4-bit weight into the bf16 Wd
+// -- six warps whose only work this is, the four epilogue warps until their
+// accumulator is ready (and again after the split exchange), and the producer
+// and MMA warps once their own work is issued.  Both streams share one launch
+// and keep HBM busy together.  The arithmetic is the standalone dequantiser's:
 // deq = bf16_rn(fp32(codebook[code] * absmax)) with one __fmul_rn, so Wd is
 // the same bit for bit.
 // A word is 8 consecutive weights: one 4-byte load of codes, one absmax (8
