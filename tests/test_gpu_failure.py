@@ -36,10 +36,13 @@ def test_stalled_pipeline_reports_timeout_and_next_call_is_correct(label):
     compare(g.results(), oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
 
 
-def test_single_cta_fallback_path_matches_oracle(monkeypatch):
+@pytest.mark.parametrize("wd_in_rankr", ["0", "1"])
+def test_single_cta_fallback_path_matches_oracle(wd_in_rankr, monkeypatch):
     """The forward and dX GEMMs also run on the single-CTA kernel (used when
-    adapter segment boundaries are not multiples of 256)."""
+    adapter segment boundaries are not multiples of 256), with the forward's
+    Wd from the separate dequantiser or from the XA launch."""
     monkeypatch.setenv("QLORA_DISABLE_PAIR", "1")
+    monkeypatch.setenv("QLORA_DQ_IN_RANKR", wd_in_rankr)
     for M, N, K, r, seg in [(300, 512, 256, 64, None), (129, 264, 128, 32, None)]:
         li = synth.make_linear(M, N, K, r, 0.5, seg_n=seg, seed=M)
         g = GpuLayer(li)
