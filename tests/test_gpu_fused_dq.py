@@ -121,3 +121,36 @@ def test_fused_dequant_stall_reports_timeout(label, monkeypatch):
     finally:
         binding.qlora_debug_stall_next_launch(None)
         binding.qlora_set_wait_limit_ns(2_000_000_000)
+
+
+def _random_shapes(n, seed=2024):
+    """Seeded shapes within the call's preconditions: ragged M, N % 8 == 0,
+    K % 64 == 0, r in 8..128 (multiple of 8), 1-3 adapter segments (all but
+    the last a multiple of 128 columns), n_seg * r <= 256."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        M = int(rng.integers(1, 600))
+        K = 64 * int(rng.integers(1, 9))
+        n_seg = int(rng.integers(1, 4))
+        r = 8 * int(rng.integers(1, 17))
+        if n_seg * r > 256:
+            continue
+        heads = [128 * int(rng.integers(1, 4)) for _ in range(n_seg - 1)]
+        last = 8 * int(rng.integers(1, 65))
+        seg = tuple(heads + [last]) if n_seg > 1 else None
+        N = sum(heads) + last
+        out.append((M, N, K, r, float(rng.choice([0.25, 0.5, 2.0])), seg))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,r,s,seg", _random_shapes(12))
+def test_random_shapes_all_weight_paths(M, N, K, r, s, seg, monkeypatch):
+    """Seeded random shapes through the three weight paths: bit-identical
+    results across them and within the oracle bounds."""
+    li = synth.make_linear(M, N, K, r, s, seg_n=seg, seed=M * 7 + N)
+    res = {m: _run(li, m, monkeypatch) for m in MODES}
+    for m in ("separate", "fused"):
+        for k in ("Y", "dX", "dA", "dB", "XA"):
+            assert np.array_equal(res[m][k], res["rankr"][k]), (m, k)
+    compare(res["rankr"], oracle_full(li), keys=("Y", "dX", "dA", "dB", "XA"))
