@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(1024, 1) quantize4_kernel(const void* __restri
   // group is converted, so two loads per thread are in flight.
   auto load8 = [&](int64_t g, float (&v)[8]) {
     if (BF16_IN) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(w) + g);
+      const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(w) + g);  // read once: streaming
       const uint32_t q4[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -201,8 +201,8 @@ __global__ void __launch_bounds__(1024, 1) quantize4_kernel(const void* __restri
         v[2 * j + 1] = __uint_as_float(q4[j] & 0xFFFF0000u);
       }
     } else {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(w) + 2 * g);
-      const float4 b = __ldg(reinterpret_cast<const float4*>(w) + 2 * g + 1);
+      const float4 a = __ldcs(reinterpret_cast<const float4*>(w) + 2 * g);  // read once: streaming
+      const float4 b = __ldcs(reinterpret_cast<const float4*>(w) + 2 * g + 1);
       v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
       v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
