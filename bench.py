@@ -316,6 +316,43 @@ def _copy_time(side, d0, d1, host_pair):
     return a.elapsed_time(b)
 
 
+def hbm_bytes_per_step(lins, wd_in_rankr: bool) -> dict:
+    """Algorithmic bytes per step of the HBM-bound launches (each operand read
+    and each output written once; bf16 = 2 B, fp32 = 4 B).  The Wd expansion
+    (codes 0.5 B + absmax 4/64 B read, 2 B written, per weight, once in the
+    forward and once in the backward) counts in the XA / G launches when they
+    write Wd, else in the dequant4 launches."""
+    wd = sum(li.N * li.K * (0.5 + 4 / 64 + 2) for li in lins)
+    return {
+        "gemm_xa": sum(2 * li.M * li.K + 2 * li.K * li.R + 4 * li.M * li.R for li in lins)
+        + (wd if wd_in_rankr else 0),
+        "gemm_g": sum(2 * li.M * li.N + 2 * li.r * li.N + 4 * li.M * li.R for li in lins)
+        + (wd if wd_in_rankr else 0),
+        "gemm_dadb": sum(2 * li.M * li.K + 2 * li.M * li.N + 4 * li.M * li.R + 4 * li.K * li.R + 4 * li.r * li.N
+                         for li in lins),
+        "dequant4": 0 if wd_in_rankr else 2 * wd,
+    }
+
+
+def hbm_bound_rows(lins, ktimes, prof_steps, hbm_peak):
+    """Per HBM-bound kernel of the step: launches, algorithmic bytes, event
+    time, GB/s and fraction of the measured copy bandwidth; `ktimes` maps a
+    kernel label to (launches, total ms) over `prof_steps` steps.  Without a
+    dequant4 launch in the step, Wd was written by the rank-r launches."""
+    wd_in_rankr = ktimes.get("dequant4", (0, 0.0))[0] == 0
+    rows = {}
+    for name, b in hbm_bytes_per_step(lins, wd_in_rankr).items():
+        n, ms = ktimes.get(name, (0, 0.0))
+        if n == 0 or ms <= 0:
+            continue
+        gbs = b * prof_steps / (ms * 1e-3) / 1e9
+        rows[name] = {"launches_per_step": n // prof_steps, "algorithmic_bytes_per_step": int(b),
+                      "ms_per_step": round(ms / prof_steps, 4), "achieved": round(gbs, 1),
+                      "frac": round(gbs / hbm_peak, 4)}
+    hbm_ms = sum(ktimes.get(k, (0, 0.0))[1] for k in ("gemm_xa", "gemm_g", "gemm_dadb", "dequant4"))
+    return rows, wd_in_rankr, hbm_ms
+
+
 def run_ours(args, rank, world):
     import torch
     from qlora_fine_tuning_gb300 import binding
@@ -634,33 +671,7 @@ def run_ours(args, rank, world):
     q_bytes = qli.N * qli.K * (4 + 0.5 + 4 / 64)
     q_gbs = q_bytes / (q_ms * 1e-3) / 1e9
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
-    # HBM-bound kernels of the step: algorithmic bytes (each operand read and
-    # each output written once) per step, against their event-timed duration.
-    # Without a dequant4 launch in the step, the bf16 Wd is written by the
-    # rank-r GEMM launch before each base GEMM (XA forward, G backward), and
-    # its expansion bytes (codes 0.5 + absmax 4/64 read, 2 written, per
-    # weight) count there.
-    wd_in_rankr = ktimes.get("dequant4", (0, 0.0))[0] == 0
-    wd_bytes = sum(li.N * li.K * (0.5 + 4 / 64 + 2) for li in lins)
-    hbm_bytes = {
-        "gemm_xa": sum(2 * li.M * li.K + 2 * li.K * li.R + 4 * li.M * li.R for li in lins)
-        + (wd_bytes if wd_in_rankr else 0),
-        "gemm_g": sum(2 * li.M * li.N + 2 * li.r * li.N + 4 * li.M * li.R for li in lins)
-        + (wd_bytes if wd_in_rankr else 0),
-        "gemm_dadb": sum(2 * li.M * li.K + 2 * li.M * li.N + 4 * li.M * li.R + 4 * li.K * li.R + 4 * li.r * li.N
-                         for li in lins),
-        "dequant4": 0 if wd_in_rankr else 2 * wd_bytes,
-    }
-    hbm_rows = {}
-    for name, b in hbm_bytes.items():
-        n, ms = ktimes.get(name, (0, 0.0))
-        if n == 0 or ms <= 0:
-            continue
-        gbs = b * prof_steps / (ms * 1e-3) / 1e9
-        hbm_rows[name] = {"launches_per_step": n // prof_steps, "algorithmic_bytes_per_step": int(b),
-                          "ms_per_step": round(ms / prof_steps, 4), "achieved": round(gbs, 1),
-                          "frac": round(gbs / hbm_peak, 4)}
-    hbm_ms = sum(ktimes.get(k, (0, 0.0))[1] for k in hbm_bytes)
+    hbm_rows, wd_in_rankr, hbm_ms = hbm_bound_rows(lins, ktimes, prof_steps, hbm_peak)
     other_rows = {
         "quantize_4bit": {"shape": f"{qli.N}x{qli.K} fp32", "ms": round(q_ms, 4), "bound": "hbm",
                           "achieved": round(q_gbs, 1), "peak": hbm_peak, "unit": "GB/s",

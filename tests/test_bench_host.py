@@ -56,3 +56,44 @@ def test_traffic_survives_a_comment_edit_but_not_a_code_edit(tmp_path):
     assert bench.pair_sources_sha256(str(src)) == base
     p.write_text(text.replace("kDqAhead = 4", "kDqAhead = 5", 1))
     assert bench.pair_sources_sha256(str(src)) != base
+
+
+def _lin(M, N, K, r, seg=None):
+    return synth.LinearInputs(M=M, N=N, K=K, r=r, s=1.0, seg_n=tuple(seg or (N,)), idx=None, absmax=None,
+                              codebook=None, X=None, A=None, B=None, dY=None)
+
+
+def test_hbm_bytes_per_step():
+    """The gate linear (M 8192, K 4096, N 14336, r 64) worked by hand: XA reads
+    X (2MK) and A (2KR) and writes XA and s*XA (4MR); the Wd expansion reads
+    0.5 + 4/64 B and writes 2 B per weight; moving the expansion between
+    launches leaves the step's total unchanged."""
+    gate = _lin(8192, 14336, 4096, 64)
+    with_wd = bench.hbm_bytes_per_step([gate], True)
+    assert with_wd["gemm_xa"] == 67108864 + 524288 + 2097152 + 150470656
+    assert with_wd["gemm_g"] == 2 * 8192 * 14336 + 2 * 64 * 14336 + 2097152 + 150470656
+    assert with_wd["dequant4"] == 0
+    sep = bench.hbm_bytes_per_step([gate], False)
+    assert sep["dequant4"] == 2 * 150470656
+    assert sum(sep.values()) == sum(with_wd.values())
+    lins = [_lin(**dict(M=kw["M"], N=kw["N"], K=kw["K"], r=kw["r"]))
+            for _, kw in synth.WORKLOADS[bench.DEFAULT_WORKLOAD]]
+    assert abs(sum(bench.hbm_bytes_per_step(lins, True).values()) / 1e9 - 2.755) < 1e-3
+
+
+def test_hbm_bound_rows_from_kernel_times():
+    gate = _lin(8192, 14336, 4096, 64)
+    steps = 10
+    # labels as the library profiler reports them: (launches, total ms)
+    kt = {"gemm_xa": (steps, 0.05 * steps), "gemm_g": (steps, 0.07 * steps), "gemm_dadb": (steps, 0.06 * steps),
+          "gemm_fwd": (steps, 0.5 * steps)}
+    rows, wd_in_rankr, hbm_ms = bench.hbm_bound_rows([gate], kt, steps, 6784.5)
+    assert wd_in_rankr and set(rows) == {"gemm_xa", "gemm_g", "gemm_dadb"}
+    b = bench.hbm_bytes_per_step([gate], True)["gemm_xa"]
+    assert rows["gemm_xa"]["launches_per_step"] == 1
+    assert abs(rows["gemm_xa"]["achieved"] - b / 0.05e-3 / 1e9) < 0.1
+    assert abs(rows["gemm_xa"]["frac"] - b / 0.05e-3 / 1e9 / 6784.5) < 1e-4
+    assert abs(hbm_ms - 0.18 * steps) < 1e-9
+    kt["dequant4"] = (2 * steps, 0.048 * steps)
+    rows, wd_in_rankr, _ = bench.hbm_bound_rows([gate], kt, steps, 6784.5)
+    assert not wd_in_rankr and rows["dequant4"]["launches_per_step"] == 2
