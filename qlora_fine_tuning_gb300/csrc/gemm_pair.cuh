@@ -348,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(FUSED_DQ ? 192 + 32 
       int mt, nt;
       pair_tile_coords(p, tile, mt, nt);
       const uint32_t acc = static_cast<uint32_t>(j & 1);
-      if (!warp_wait(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
+      if (!warp_wait_sleepy(&tfull[acc], static_cast<uint32_t>(j >> 1) & 1u, p.timeout_ns, abort_flag)) {
         if (lane == 0) {
           if (!*abort_flag) report(p, 4u);
           *abort_flag = 1;
